@@ -1,0 +1,64 @@
+"""The whole MoE expert layer: route -> permute -> expert FFN -> combine (+ shared expert).
+
+The shared (always-on) expert is an FFN of the same shape applied to every token
+with weight 1 and no gate (reading: the pages describe no shared expert; the
+large-layer workload adds one).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .ffn import combine, expert_ffn, swiglu_ffn
+from .formats import decode_blocks
+from .permute import permute
+from .route import route
+
+
+def _x_fp64(x_bf16_bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values."""
+    b = np.asarray(x_bf16_bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def layer(x_bits, logits, k, qtype, w13, w2, shared_w13=None, shared_w2=None):
+    """Full layer on all tokens.
+
+    x_bits uint16 bf16 [T, H]; logits float32 [T, E]; w13 uint8 [E, 2I, H/32, blk];
+    w2 uint8 [E, H, I/32, blk].  Returns a dict with ids, w, offsets, sorted_pair,
+    inv_pos, y_perm [P, H] and out [T, H] (fp64)."""
+    x = _x_fp64(x_bits)
+    E = w13.shape[0]
+    ids, w = route(logits, k)
+    offsets, sorted_pair, inv_pos = permute(ids, E)
+    y = expert_ffn(x, k, offsets, sorted_pair,
+                   lambda e: decode_blocks(w13[e], qtype), lambda e: decode_blocks(w2[e], qtype))
+    sh = None
+    if shared_w13 is not None:
+        sh = swiglu_ffn(x, decode_blocks(shared_w13[0], qtype), decode_blocks(shared_w2[0], qtype))
+    out = combine(y, w, inv_pos, sh)
+    return dict(ids=ids, w=w, offsets=offsets, sorted_pair=sorted_pair, inv_pos=inv_pos,
+                y_perm=y, out=out, shared_y=sh)
+
+
+def layer_rows(x_bits, logits, k, qtype, w13, w2, rows, shared_w13=None, shared_w2=None):
+    """Layer output for a subset of tokens, by the per-token definition.
+
+    A token's output depends only on its own activations and logits:
+    out[t] = sum_j w[t, j] * FFN_{ids[t, j]}(x[t]) (+ FFN_shared(x[t])).
+    Returns (ids [n, k], w [n, k], out fp64 [n, H]) for the tokens in ``rows``."""
+    rows = np.asarray(rows, dtype=np.int64)
+    x = _x_fp64(np.asarray(x_bits)[rows])
+    ids, w = route(np.asarray(logits)[rows], k)
+    n, H = x.shape
+    out = np.zeros((n, H))
+    cache13, cache2 = {}, {}
+    for i in range(n):
+        for j in range(k):
+            e = int(ids[i, j])
+            if e not in cache13:
+                cache13[e] = decode_blocks(w13[e], qtype)
+                cache2[e] = decode_blocks(w2[e], qtype)
+            out[i] += w[i, j] * swiglu_ffn(x[i:i + 1], cache13[e], cache2[e])[0]
+    if shared_w13 is not None:
+        out += swiglu_ffn(x, decode_blocks(shared_w13[0], qtype), decode_blocks(shared_w2[0], qtype))
+    return ids, w, out

@@ -1,0 +1,233 @@
+"""Seeded generators and block encoders for the MoE layer workloads.
+
+Weights are drawn N(0, std) in float32 and encoded into canonical blocks:
+
+* GGUF Q4_0 block (18 bytes): little-endian fp16 scale ``d`` then 16 bytes of
+  codes; element ``i < 16`` is the low nibble of code byte ``i`` and element
+  ``i >= 16`` the high nibble of code byte ``i - 16``.  A decoder maps a code
+  ``q`` to ``(q - 8) * d``.  (GGUF is the llama.cpp format the FreeToken pages
+  name: "FreeToken：在桌面运行大规模模型的本地推理引擎", section 开源生态中的位置,
+  and the Q4_0 bank of "深入FreeToken架构…全链路剖析" §五/§六.)
+* OCP MXFP4 block (17 bytes): one E8M0 scale byte then 16 code bytes in the
+  same nibble order; codes are E2M1 (OCP Microscaling Formats v1.0).
+
+The encoders below only produce bytes; decoding them is the job of the oracle
+on one side and the CUDA kernels on the other.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+import zlib
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+QTYPE_BLOCK_BYTES = {"q4_0": 18, "mxfp4": 17}
+BLOCK = 32
+
+# Workloads: the shapes, value distributions and seeds of the layer configs.
+CONFIGS = {
+    "tiny": dict(H=256, I=128, E=8, k=2, T=64, qtype="q4_0", zipf=0.0, no_ties=True, seed=0),
+    "decode": dict(H=2048, I=768, E=128, k=8, T=64, T_sweep=(1, 4, 16, 64), qtype="q4_0",
+                   zipf=0.0, no_ties=False, seed=0),
+    "prefill": dict(H=2048, I=768, E=128, k=8, T=4096, qtype="q4_0", qtypes=("q4_0", "mxfp4"),
+                    zipf=1.0, no_ties=False, seed=0),
+    "large": dict(H=7168, I=2048, E=256, k=8, T=2048, T_total=16384, decode_T=32, qtype="mxfp4",
+                  shared=True, zipf=1.0, no_ties=False, seed=0),
+    "stream": dict(H=2048, I=768, E=128, k=8, T=1, layers=48, slots=32, steps=2048, p_repeat=0.7,
+                   qtype="q4_0", zipf=1.0, seed=0),
+}
+
+
+def _rng(seed: int, *tags) -> np.random.Generator:
+    """Independent stream per (seed, tags); tags may be strings or ints."""
+    ent = [int(seed) & 0xFFFFFFFF]
+    for t in tags:
+        ent.append(zlib.crc32(t.encode()) if isinstance(t, str) else int(t) & 0xFFFFFFFF)
+    return np.random.default_rng(ent)
+
+
+# ----------------------------------------------------------------------------- bf16 inputs
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (round to nearest even); returns the uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def gen_x_bf16(seed: int, T: int, H: int, tag: str = "x") -> np.ndarray:
+    """Activations ~N(0,1) rounded to bf16; uint16 bits [T, H]."""
+    x = _rng(seed, tag, T, H).standard_normal((T, H), dtype=np.float32)
+    return f32_to_bf16_bits(x)
+
+
+def zipf_bias(E: int, s: float) -> np.ndarray:
+    """Expert popularity skew added to router logits: -s * ln(e + 1) (expert 0 most popular)."""
+    return -s * np.log(np.arange(1, E + 1, dtype=np.float64))
+
+
+def gen_logits(seed: int, T: int, E: int, zipf: float = 0.0, no_ties: bool = False,
+               tag: str = "logits") -> np.ndarray:
+    """Router logits fp32 [T, E] = N(0,1) (+ log-Zipf bias).  With ``no_ties`` a token's
+    row is redrawn until its E values are pairwise distinct."""
+    rng = _rng(seed, tag, T, E)
+    lg = rng.standard_normal((T, E), dtype=np.float32)
+    if no_ties:
+        for t in range(T):
+            while len(np.unique(lg[t])) != E:
+                lg[t] = rng.standard_normal(E, dtype=np.float32)
+    if zipf:
+        lg = (lg.astype(np.float64) + zipf_bias(E, zipf)[None, :]).astype(np.float32)
+    return lg
+
+
+# ----------------------------------------------------------------------------- encoders
+def quantize_q4_0(w: np.ndarray) -> np.ndarray:
+    """Encode float32 [..., K] (K % 32 == 0) into Q4_0 blocks uint8 [..., K/32, 18].
+
+    Per block: m = the element of largest magnitude (first on ties), d = m / -8,
+    q = clamp(floor(x * (1/d) + 8.5), 0, 15); d is stored as fp16 (round to nearest).
+    An all-zero block stores d = 0 and q = 8."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    assert K % BLOCK == 0
+    lead = w.shape[:-1]
+    b = w.reshape(-1, BLOCK)
+    n = b.shape[0]
+    idx = np.argmax(np.abs(b), axis=1)
+    m = b[np.arange(n), idx]
+    d = (m / np.float32(-8.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(d != 0, np.float32(1.0) / np.where(d != 0, d, 1), np.float32(0)).astype(np.float32)
+    q = np.clip(np.floor(b * inv[:, None] + np.float32(8.5)), 0, 15).astype(np.uint8)
+    out = np.empty((n, 18), dtype=np.uint8)
+    out[:, 0:2] = d.astype(np.float16).view(np.uint8).reshape(n, 2)
+    out[:, 2:18] = q[:, :16] | (q[:, 16:] << 4)
+    return out.reshape(*lead, K // BLOCK, 18)
+
+
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def quantize_mxfp4(w: np.ndarray) -> np.ndarray:
+    """Encode float32 [..., K] into MXFP4 blocks uint8 [..., K/32, 17].
+
+    Per block: shared exponent u = floor(log2(amax)) - 2 clamped to [-127, 127]
+    (scale byte u + 127; amax == 0 gives byte 127 and zero codes); each element
+    x / 2^u is rounded to the nearest E2M1 magnitude (ties to the even code),
+    saturating at 6; bit 3 of the code is the sign."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    assert K % BLOCK == 0
+    lead = w.shape[:-1]
+    b = w.reshape(-1, BLOCK).astype(np.float64)
+    n = b.shape[0]
+    amax = np.max(np.abs(b), axis=1)
+    with np.errstate(divide="ignore"):
+        u = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0.0)
+    u = np.clip(u, -127, 127)
+    v = b / np.exp2(u)[:, None]
+    mag = np.minimum(np.abs(v), 6.0)
+    dist = np.abs(mag[..., None] - _E2M1_GRID)
+    c = np.argmin(dist, axis=-1)  # lower code on a tie
+    c1 = np.minimum(c + 1, 7)
+    tie = (np.take_along_axis(dist, c1[..., None], -1)[..., 0] == np.take_along_axis(dist, c[..., None], -1)[..., 0]) & (c1 != c)
+    c = np.where(tie & (c % 2 == 1), c1, c)  # round half to even code
+    sign = ((v < 0) & (c != 0)).astype(np.uint8)
+    code = (c.astype(np.uint8) | (sign << 3)).astype(np.uint8)
+    out = np.empty((n, 17), dtype=np.uint8)
+    out[:, 0] = (u + 127).astype(np.uint8)
+    out[:, 1:17] = code[:, :16] | (code[:, 16:] << 4)
+    return out.reshape(*lead, K // BLOCK, 17)
+
+
+_ENCODERS = {"q4_0": quantize_q4_0, "mxfp4": quantize_mxfp4}
+
+
+def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
+                       std: float = 0.02, distinct: int | None = None,
+                       threads: int = 8) -> np.ndarray:
+    """Canonical block bytes uint8 [E, N, K/32, block] of N(0, std) weights.
+
+    Expert e draws from its own stream (seed, tag, e).  With ``distinct`` < E only that
+    many expert matrices are drawn and expert e holds a copy of matrix e % distinct
+    (used for the largest banks, where drawing every expert would dominate run time)."""
+    enc = _ENCODERS[qtype]
+    nb = QTYPE_BLOCK_BYTES[qtype]
+    out = np.empty((E, N, K // BLOCK, nb), dtype=np.uint8)
+    D = E if distinct is None else min(distinct, E)
+
+    def one(e):
+        w = _rng(seed, tag, qtype, e, N, K).standard_normal((N, K), dtype=np.float32)
+        w *= np.float32(std)
+        out[e] = enc(w)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, range(D)))
+    for e in range(D, E):
+        out[e] = out[e % D]
+    return out
+
+
+@dataclasses.dataclass
+class LayerInputs:
+    """One layer's inputs in canonical form (host numpy)."""
+    H: int
+    I: int
+    E: int
+    k: int
+    T: int
+    qtype: str
+    x: np.ndarray          # uint16 bf16 bits [T, H]
+    logits: np.ndarray     # float32 [T, E]
+    w13: np.ndarray        # uint8 [E, 2I, H/32, blk]; rows [0, I) gate, [I, 2I) up
+    w2: np.ndarray         # uint8 [E, H, I/32, blk]
+    shared_w13: np.ndarray | None = None  # uint8 [1, 2I, H/32, blk]
+    shared_w2: np.ndarray | None = None   # uint8 [1, H, I/32, blk]
+
+
+def make_layer(H: int, I: int, E: int, k: int, T: int, qtype: str = "q4_0", seed: int = 0,
+               zipf: float = 0.0, no_ties: bool = False, shared: bool = False,
+               distinct: int | None = None, std: float = 0.02, x_tag: str = "x",
+               logit_tag: str = "logits", **_unused) -> LayerInputs:
+    w13 = gen_expert_weights(seed, "w13", E, 2 * I, H, qtype, std, distinct)
+    w2 = gen_expert_weights(seed, "w2", E, H, I, qtype, std, distinct)
+    sw13 = sw2 = None
+    if shared:
+        sw13 = gen_expert_weights(seed, "shared_w13", 1, 2 * I, H, qtype, std)
+        sw2 = gen_expert_weights(seed, "shared_w2", 1, H, I, qtype, std)
+    return LayerInputs(H, I, E, k, T, qtype,
+                       gen_x_bf16(seed, T, H, x_tag),
+                       gen_logits(seed, T, E, zipf, no_ties, logit_tag),
+                       w13, w2, sw13, sw2)
+
+
+def stream_trace(seed: int, steps: int, layers: int, E: int, k: int, p_repeat: float,
+                 s: float) -> np.ndarray:
+    """Batch-1 decode expert trace int32 [steps, layers, k].
+
+    Step 0 draws; afterwards each (step, layer) repeats that layer's previous ids with
+    probability p_repeat, else draws k distinct ids from Zipf(s) over E experts by
+    rejection (redraw an id already taken)."""
+    rng = _rng(seed, "trace", steps, layers, E, k)
+    p = 1.0 / np.power(np.arange(1, E + 1, dtype=np.float64), s)
+    cdf = np.cumsum(p / p.sum())
+    out = np.empty((steps, layers, k), dtype=np.int32)
+    for st in range(steps):
+        for l in range(layers):
+            if st > 0 and rng.random() < p_repeat:
+                out[st, l] = out[st - 1, l]
+                continue
+            got: list[int] = []
+            while len(got) < k:
+                e = int(np.searchsorted(cdf, rng.random(), side="right"))
+                e = min(e, E - 1)
+                if e not in got:
+                    got.append(e)
+            out[st, l] = got
+    return out

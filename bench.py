@@ -1,0 +1,353 @@
+"""Benchmark of the quantized MoE expert layer on B300 (one JSON line on rank 0).
+
+Default workload: the decode layer (hidden 2048, expert intermediate 768, 128
+experts, top-8, Q4_0) at a batch of 64 tokens.  One step = one full layer pass
+(route -> permute -> expert FFN -> combine) over one batch, inputs resident in
+HBM.  Between timed steps a 512 MB buffer is written to flush the 126 MB L2, and
+only the layer itself sits inside the per-step CUDA events.
+
+--impl reference times the fp64 CPU oracle on the same workload instead.
+Multi-GPU (torchrun): independent replicas, one per rank, no collective on the
+data path; value = tokens of all ranks / max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import CONFIGS, gen_logits, make_layer  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                r = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                    "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                   timeout=5)
+                if r.returncode == 0 and r.stdout.strip():
+                    self.rows.append([s.strip() for s in r.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+def unique_experts(ids: np.ndarray) -> int:
+    return int(len(np.unique(ids)))
+
+
+def oracle_cpu_run(L, sample_T: int, reps: int = 1):
+    """Time the fp64 oracle on the first sample_T tokens of the workload."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except ImportError:  # numpy's bundled OpenBLAS uses one thread per core by default
+        threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.layer(L.x[:sample_T], L.logits[:sample_T], L.k, L.qtype, L.w13, L.w2,
+                     L.shared_w13, L.shared_w2)
+    dt = time.perf_counter() - t0
+    return sample_T * reps / dt, threads, dt
+
+
+def run_reference(args, cfg, L, world, rank):
+    """--impl reference: the fp64 oracle as it stands, on this host's cores."""
+    if rank != 0:
+        return
+    sample_T = min(L.T, args.ref_tokens)
+    vals = []
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; keep the step count honest
+    t_all = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        v, threads, _ = oracle_cpu_run(L, sample_T)
+        vals.append(v)
+    dt = time.perf_counter() - t_all
+    value = sample_T * args.steps / dt
+    sample = f"{sample_T} tokens of the {L.T}-token batch per step (full oracle layer, fp64)"
+    line = {"impl": "reference", "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["workload"]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "tiny"])
+    ap.add_argument("--T", type=int, default=None, help="tokens per step (default: config's)")
+    ap.add_argument("--qtype", default=None)
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    c = dict(CONFIGS[args.config])
+    if args.T:
+        c["T"] = args.T
+    if args.qtype:
+        c["qtype"] = args.qtype
+    cfg = dict(c)
+    cfg["workload"] = (f"{args.config} layer H{c['H']} I{c['I']} E{c['E']} top-{c['k']} "
+                       f"{c['qtype']} T{c['T']}")
+    # replicas draw different activations / logits, same weight distribution
+    L = make_layer(**{**c, "seed": c.get("seed", 0) + rank})
+
+    if args.impl == "reference":
+        run_reference(args, cfg, L, world, rank)
+        return
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev)
+    T, k = L.T, L.k
+    x = torch.from_numpy(L.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(L.logits).to(dev)
+    out = torch.empty((T, L.H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.forward(lg, x, k, out=out, ids_out=ids, w_out=wts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    U = unique_experts(ids.cpu().numpy())
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    my_ms = float(np.sum(step_ms))
+    max_ms = my_ms
+    if pg:
+        t = torch.tensor([my_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        max_ms = float(t.item())
+    tokens_all = T * args.steps * world
+    value = tokens_all / (max_ms / 1e3)
+
+    # ---- dominant kernel: the expert FFN step (gate/up+SwiGLU GEMV, down GEMV),
+    # timed alone on the same stream with its inputs from the route/permute above
+    E, H, I = L.E, L.H, L.I
+    P = T * k
+    ws_ffn_n = F.ftmoe_ffn_workspace_bytes(T, k, E, H, I)
+    ws_ffn = torch.empty(max(ws_ffn_n, 256), dtype=torch.uint8, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    inv = torch.empty(P, dtype=torch.int32, device=dev)
+    pws_n = F.ftmoe_permute_workspace_bytes(T, k, E)
+    pws = torch.empty(max(pws_n, 256), dtype=torch.uint8, device=dev)
+    F.ftmoe_permute(ids, T, k, E, offs, sp, inv, pws, pws_n)
+    y_perm = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        F.ftmoe_expert_ffn(m.weights, x, T, k, offs, sp, y_perm, ws_ffn, ws_ffn_n)
+    kt = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        F.ftmoe_expert_ffn(m.weights, x, T, k, offs, sp, y_perm, ws_ffn, ws_ffn_n)
+        b.record(stream)
+        kt.append((a, b))
+    torch.cuda.synchronize()
+    ffn_ms = float(np.mean([a.elapsed_time(b) for a, b in kt]))
+    blob = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
+    alg_bytes = U * blob + P * H * 2 + P * H * 2 + T * H * 2 + P * I * 2 * 2
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "expert FFN (gate/up+SwiGLU GEMV, down GEMV)",
+                "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_kind": f"{pk_kind} hbm_gbs (copy)", "traffic": None,
+                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": ffn_ms, "unique_experts": U}
+    layer_bytes = alg_bytes + T * E * 4
+    layer_frac = layer_bytes / (np.mean(step_ms) / 1e3) / 1e9 / hbm
+
+    # ---- end to end through the C ABI with host buffers
+    x_h = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    lg_h = torch.from_numpy(L.logits).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(lg)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        m.forward(lg_d, x_d, k, out=out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    ee = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        ee.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in ee]))
+    e2e_ms_max = e2e_ms
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms_max = float(t.item())
+    e2e_val = tokens_all / (e2e_ms_max / 1e3)
+
+    # ---- decode sweep over the other batch sizes (informative)
+    sweep = {}
+    if not args.no_sweep and args.config == "decode":
+        for Ts in CONFIGS["decode"]["T_sweep"]:
+            if Ts == T:
+                sweep[str(Ts)] = {"tokens_per_s": value, "ms": float(np.mean(step_ms))}
+                continue
+            xs = x[:Ts].contiguous()
+            lgs = torch.from_numpy(gen_logits(c.get("seed", 0) + rank, Ts, E)).to(dev)
+            os_ = torch.empty((Ts, H), dtype=torch.bfloat16, device=dev)
+            for _ in range(3):
+                m.forward(lgs, xs, k, out=os_)
+            ev = []
+            for _ in range(max(10, args.steps)):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                m.forward(lgs, xs, k, out=os_)
+                b.record(stream)
+                ev.append((a, b))
+            torch.cuda.synchronize()
+            ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+            sweep[str(Ts)] = {"tokens_per_s": Ts / (ms / 1e3), "ms": ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_T = min(T, args.ref_tokens)
+        v, threads, dt = oracle_cpu_run(L, sample_T)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"one oracle layer pass over {sample_T} tokens of the workload ({dt:.1f} s)"}
+
+    launches_per_step = 1 + (1 if P <= 16384 else 3) + 2 + 1
+    if rank == 0:
+        line = {
+            "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(step_ms)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
+            "config": {"workload": cfg["workload"], "H": L.H, "I": L.I, "E": L.E, "k": k, "T": T,
+                       "qtype": L.qtype, "parallelism": f"replicas{world}",
+                       "l2": "flushed between steps (512 MB write)"},
+            "roofline": roofline,
+            "layer_hbm_frac": layer_frac,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "decode_sweep": sweep or None,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

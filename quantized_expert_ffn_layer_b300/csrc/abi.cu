@@ -40,19 +40,26 @@ bool tke_ok(int T, int k, int E) {
 }
 
 // Workspace carve-up shared by ftmoe_expert_ffn and ftmoe_layer.
+// Workspace of the FFN: [gemv scratch (zero region first)][h_act][gemm scratch].
 struct FfnWs {
+  void* gemv_ws;
+  size_t gemv_zero_bytes;
   uint16_t* h_act;
   void* gemm_ws;
   size_t gemm_bytes;
 };
 size_t ffn_ws_bytes(int T, int k, int E, int H, int I) {
   const long long P = (long long)T * k;
-  return align256((size_t)P * I * 2) + align256(ffn_gemm_ws_bytes(T, k, E, H, I));
+  return align256(ffn_gemv_ws_bytes(T, k, E, H, I)) + align256((size_t)P * I * 2) +
+         align256(ffn_gemm_ws_bytes(T, k, E, H, I));
 }
 FfnWs carve_ffn(void* ws, int T, int k, int E, int H, int I) {
   const long long P = (long long)T * k;
   char* b = (char*)ws;
   FfnWs w;
+  w.gemv_ws = b;
+  w.gemv_zero_bytes = ffn_gemv_zero_bytes(T, k, E, H, I);
+  b += align256(ffn_gemv_ws_bytes(T, k, E, H, I));
   w.h_act = (uint16_t*)b;
   b += align256((size_t)P * I * 2);
   w.gemm_ws = b;
@@ -79,7 +86,8 @@ bool weights_ok(const ftmoe_weights* w) {
 
 ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, int k,
                      const int32_t* offsets, const int32_t* sorted_pair, uint16_t* y_perm,
-                     const void* w13, const void* w2, bool use_table, void* ws, cudaStream_t st) {
+                     const void* w13, const void* w2, bool use_table, void* ws, bool ws_zeroed,
+                     cudaStream_t st) {
   FfnProblem pb{};
   pb.qtype = wts->qtype;
   pb.E = E;
@@ -111,7 +119,7 @@ ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, 
     if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
     if (path == FTMOE_PATH_GEMM) return FTMOE_ERR_UNSUPPORTED;
   }
-  return from_cuda(launch_ffn_gemv(pb, st));
+  return from_cuda(launch_ffn_gemv(pb, fw.gemv_ws, ws_zeroed, st));
 }
 }  // namespace
 
@@ -185,7 +193,7 @@ ftmoe_status ftmoe_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   if (!di) return FTMOE_ERR_CUDA;
   if (T == 0) return from_cuda(cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), (cudaStream_t)stream));
   return from_cuda(launch_permute(ids, T, k, E, offsets, sorted_pair, inv_pos, ws, di->status,
-                                  (cudaStream_t)stream));
+                                  nullptr, 0, (cudaStream_t)stream));
 }
 
 size_t ftmoe_expert_blob_bytes(int qtype, int H, int I) {
@@ -214,7 +222,7 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_weights* wts, const uint16_t* x, int T
   if (ws_bytes < ffn_ws_bytes(T, k, wts->E, wts->H, wts->I) || !ws) return FTMOE_ERR_WORKSPACE;
   if (!device_info()) return FTMOE_ERR_CUDA;
   return run_ffn(wts, wts->E, x, T, k, offsets, sorted_pair, y_perm, wts->w13, wts->w2,
-                 wts->expert_blob != nullptr, ws, (cudaStream_t)stream);
+                 wts->expert_blob != nullptr, ws, false, (cudaStream_t)stream);
 }
 
 ftmoe_status ftmoe_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_pos,
@@ -286,16 +294,18 @@ ftmoe_status ftmoe_layer(const ftmoe_weights* wts, const float* logits, const ui
   float* w = w_out ? w_out : L.w;
   cudaError_t e = launch_route(logits, T, E, k, ids, w, st);
   if (e != cudaSuccess) return FTMOE_ERR_CUDA;
-  e = launch_permute(ids, T, k, E, L.offsets, L.sorted_pair, L.inv_pos, L.perm_ws, di->status, st);
+  // the permutation kernel also clears the FFN scratch that must start at zero
+  e = launch_permute(ids, T, k, E, L.offsets, L.sorted_pair, L.inv_pos, L.perm_ws, di->status,
+                     L.ffn_ws, ffn_gemv_zero_bytes(T, k, E, H, I), st);
   if (e != cudaSuccess) return FTMOE_ERR_CUDA;
   ftmoe_status s = run_ffn(wts, E, x, T, k, L.offsets, L.sorted_pair, L.y_perm, wts->w13, wts->w2,
-                           wts->expert_blob != nullptr, L.ffn_ws, st);
+                           wts->expert_blob != nullptr, L.ffn_ws, true, st);
   if (s != FTMOE_OK) return s;
   if (shared) {
     set_pair_kernel<<<1, 1, 0, st>>>(L.sh_offsets, 0, T);
     if (cudaGetLastError() != cudaSuccess) return FTMOE_ERR_CUDA;
     s = run_ffn(wts, 1, x, T, 1, L.sh_offsets, nullptr, L.y_sh, wts->shared_w13, wts->shared_w2,
-                false, L.ffn_ws, st);
+                false, L.ffn_ws, false, st);
     if (s != FTMOE_OK) return s;
   }
   return from_cuda(launch_combine(L.y_perm, w, L.inv_pos, shared ? L.y_sh : nullptr, T, k, H, out, st));

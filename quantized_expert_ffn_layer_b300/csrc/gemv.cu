@@ -2,41 +2,42 @@
 // 4-bit expert weights with in-register decode (the ExpertFFN of the FreeToken
 // architecture walkthrough §五, on GGUF Q4_0 / MXFP4 banks, §六).
 //
-// Persistent CTAs: one producer warp streams 16-row x 64-column weight records with
-// 1-D bulk copies (TMA) into a ring of shared-memory stages; eight consumer warps
-// turn the codes into exact bf16 (q - 8, or the E2M1 value) and feed them as the A
-// operand of m16n8k16 MMAs whose B operand is up to 8 token rows; after the two
-// k-steps of a quantization block the partial sums are scaled by that block's scale
-// in fp32.  So the only roundings are the fp32 accumulation, the bf16 h between the
-// projections and the bf16 output.
+// Work item = (active expert, two 16-row tiles, a group of reduction parts): the
+// gate and up tile of one group of 16 features (gate/up projection), or two tiles of
+// 16 output rows (down projection).  Every warp owns its items outright: its lane 0
+// streams the items' 16-row x 64-column weight records with 1-D bulk copies (TMA)
+// into the warp's own ring of shared-memory stages, and the warp turns the codes
+// into exact bf16 (q - 8, or the E2M1 value) as the A operand of m16n8k16 MMAs
+// whose B operand (up to 8 token rows) is loaded into registers one stage ahead.
+// After the two k-steps of a quantization block the partial sums are scaled by the
+// block's scale in fp32, so the only roundings are the fp32 accumulation, the bf16
+// h between the projections and the bf16 output.
 //
-// Unit of work = (active expert, two 16-row tiles): gate and up tile of one group of
-// 16 features (gate/up), or two tiles of 16 output rows (down).  A unit's records
-// arrive in chunks of up to 16 slabs (64 reduction elements each); consumer warp w
-// works on slab w of every chunk for both tiles, with its token fragment (up to 8
-// token rows) loaded into registers one chunk ahead, and the 16 partial sums of a
-// tile are added in shared memory at the end of the unit.
+// The reduction dimension is cut into fixed parts of 512 elements; each part is
+// summed from zero and the parts are added in order.  For small batches the parts
+// of one tile pair are spread over several warps, which write per-part sums to
+// scratch; the last warp to arrive adds them in part order.  Either way the result
+// is bit-identical, so a token's output does not depend on the batch it is in.
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
 
 namespace ftmoe {
 
-constexpr int GV_CONS_WARPS = 16;
-constexpr int GV_THREADS = (GV_CONS_WARPS + 1) * 32;
-constexpr int GV_CH = 16;      // slabs per chunk (one per consumer warp)
-constexpr int GV_NSTAGE = 8;   // 8 x 18 KB of weights in flight per SM
+constexpr int GW_WARPS = 8;     // warps per CTA (2 CTAs per SM)
+constexpr int GW_THREADS = GW_WARPS * 32;
+constexpr int GW_SL = 4;        // slabs (64 reduction elements) per stage
+constexpr int GW_NS = 3;        // stages per warp
+constexpr int GW_PS = 8;        // slabs per fixed reduction part
+constexpr int GW_KPMAX = 16;    // most warps sharing one tile pair
 
 template <int QT>
-struct GvSmem {
-  static constexpr int STAGE = 2 * GV_CH * rec_bytes(QT);
-  uint8_t stage[GV_NSTAGE][STAGE];
-  float red[2][GV_CONS_WARPS][2][4][32];  // [parity][warp][tile][C fragment][lane]
-  uint64_t full[GV_NSTAGE];
-  uint64_t empty[GV_NSTAGE];
-  uint64_t ebar;  // all consumer warps meet here once per unit epilogue
-  int act[1024];
-  int wsum[GV_THREADS / 32];
+struct GwSmem {
+  static constexpr int STAGE = 2 * GW_SL * rec_bytes(QT);
+  uint8_t stage[GW_WARPS][GW_NS][STAGE];
+  uint64_t full[GW_WARPS][GW_NS];
+  int16_t act[1024];
+  int wsum[GW_WARPS];
 };
 
 struct GemvArgs {
@@ -52,8 +53,12 @@ struct GemvArgs {
   long long table_off;   // offset of this projection inside a blob
   int S;                 // slabs per row
   int K;                 // reduction length
+  int NP;                // fixed parts: ceil(S / GW_PS)
   int up_rt;             // gate/up: first row tile of the up half (I / 16)
   int units_per_expert;  // gate/up: I / 16; down: H / 32
+  int kp;                // part groups (warps) per unit
+  int* counters;         // [units] arrival counters (kp > 1), zero on entry
+  float* partials;       // [units][NP][256] per-part sums (kp > 1)
   int* status;
 };
 
@@ -70,12 +75,11 @@ struct WithTable {
 };
 
 // Ordered list of experts with at least one row, built by every CTA from offsets.
-__device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, int* s_act,
+__device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, int16_t* s_act,
                                                  int* s_wsum) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  constexpr int NW = GV_THREADS / 32;
   int nact = 0;
-  for (int e0 = 0; e0 < E; e0 += GV_THREADS) {
+  for (int e0 = 0; e0 < E; e0 += GW_THREADS) {
     const int e = e0 + threadIdx.x;
     const bool f = e < E && offsets[e + 1] > offsets[e];
     const unsigned b = __ballot_sync(0xffffffffu, f);
@@ -83,11 +87,11 @@ __device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, 
     __syncthreads();
     int before = nact, tot = 0;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
+    for (int w = 0; w < GW_WARPS; ++w) {
       if (w < wid) before += s_wsum[w];
       tot += s_wsum[w];
     }
-    if (f) s_act[before + __popc(b & ((1u << lane) - 1u))] = e;
+    if (f) s_act[before + __popc(b & ((1u << lane) - 1u))] = (int16_t)e;
     nact += tot;
     __syncthreads();
   }
@@ -117,139 +121,160 @@ __device__ __forceinline__ void load_scales(const uint8_t* rec, int g, float (&s
   }
 }
 
-struct UnitInfo {
-  int e, r0, n_e, tile0, tile1;
+// A warp's position in its flattened sequence of stages: item -> round -> stage.
+struct Cursor {
+  int item;            // unit * kp + group
+  int unit;            // active expert * units_per_expert + sub
+  int r0, n_e, tile0, tile1;
+  int s0, s1;          // slab range of the item's group of parts
+  int r, sp;           // round (8 tokens), first slab of the stage
+  const uint8_t* w0;   // records of tile0 / tile1
+  const uint8_t* w1;
+  const uint16_t* brow;  // this lane's token row (B operand) for the round
 };
 
 template <int MODE>
-__device__ __forceinline__ UnitInfo unit_info(const GemvArgs& a, const int* s_act, int unit) {
-  UnitInfo u;
-  const int ui = unit / a.units_per_expert;
-  const int sub = unit - ui * a.units_per_expert;
-  u.e = s_act[ui];
-  u.r0 = a.offsets[u.e];
-  u.n_e = a.offsets[u.e + 1] - u.r0;
-  if (MODE == 0) {
-    u.tile0 = sub;
-    u.tile1 = a.up_rt + sub;
-  } else {
-    u.tile0 = 2 * sub;
-    u.tile1 = 2 * sub + 1;
+__device__ __forceinline__ void cursor_row(Cursor& c, const GemvArgs& a, int g) {
+  const int rr = min(8 * c.r + g, c.n_e - 1);  // padded lanes re-read a valid row
+  long long row;
+  if (MODE == 0) row = a.sorted_pair ? a.sorted_pair[c.r0 + rr] / a.k : (c.r0 + rr);
+  else row = c.r0 + rr;
+  c.brow = a.act + row * a.act_ld;
+}
+
+template <int MODE, class Tab>
+__device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const Tab& tab,
+                                            const int16_t* s_act, int total, int g) {
+  if (c.item >= total) return;
+  c.unit = c.item / a.kp;
+  const int grp = c.item - c.unit * a.kp;
+  const int ui = c.unit / a.units_per_expert;
+  const int sub = c.unit - ui * a.units_per_expert;
+  const int e = s_act[ui];
+  c.r0 = a.offsets[e];
+  c.n_e = a.offsets[e + 1] - c.r0;
+  c.tile0 = MODE == 0 ? sub : 2 * sub;
+  c.tile1 = MODE == 0 ? a.up_rt + sub : 2 * sub + 1;
+  c.s0 = (grp * a.NP / a.kp) * GW_PS;
+  c.s1 = min(((grp + 1) * a.NP / a.kp) * GW_PS, a.S);
+  c.r = 0;
+  c.sp = c.s0;
+  const uint8_t* wexp = tab.get(e, a);
+  c.w0 = wexp;
+  c.w1 = wexp;
+  cursor_row<MODE>(c, a, g);
+}
+
+// Next stage; returns true when the (item, round) just left is complete.
+template <int MODE, class Tab>
+__device__ __forceinline__ bool cursor_next(Cursor& c, const GemvArgs& a, const Tab& tab,
+                                            const int16_t* s_act, int total, int nwarps, int g) {
+  c.sp += GW_SL;
+  if (c.sp < c.s1) return false;
+  c.sp = c.s0;
+  if (++c.r < (c.n_e + 7) / 8) {
+    cursor_row<MODE>(c, a, g);
+    return true;
   }
-  return u;
+  c.item += nwarps;
+  cursor_load<MODE>(c, a, tab, s_act, total, g);
+  return true;
 }
 
 template <int QT, int MODE, class Tab>
-__global__ void __launch_bounds__(GV_THREADS, 1) gemv_ffn_kernel(const GemvArgs a,
-                                                                 const __grid_constant__ Tab tab) {
-  using SM = GvSmem<QT>;
+__global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs a,
+                                                              const __grid_constant__ Tab tab) {
+  using SM = GwSmem<QT>;
   constexpr int RB = rec_bytes(QT);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int g = lane >> 2, c4 = lane & 3;
 
   if (MODE == 0) pdl_wait();  // offsets come from the permutation kernel
   pdl_launch_dependents();
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < GV_NSTAGE; ++i) {
-      mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], GV_CONS_WARPS);
-    }
-    mbar_init(&sm.ebar, GV_CONS_WARPS);
-    fence_barrier_init();
-  }
+  if (lane == 0)
+    for (int i = 0; i < GW_NS; ++i) mbar_init(&sm.full[wid][i], 1);
+  fence_barrier_init();
   const int nact = build_active_list(a.offsets, a.E, sm.act, sm.wsum);  // contains __syncthreads
-  const int total = nact * a.units_per_expert;
-  // contiguous share of the units per CTA
-  const int u_begin = (int)((long long)total * blockIdx.x / gridDim.x);
-  const int u_end = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
-  const int nchunk = (a.S + GV_CH - 1) / GV_CH;
+  const int total = nact * a.units_per_expert * a.kp;
+  const int nwarps = gridDim.x * GW_WARPS;
+  const int gw = blockIdx.x * GW_WARPS + wid;
   const bool ragged = (a.K & 63) != 0;
+  uint8_t (*stage)[SM::STAGE] = sm.stage[wid];
+  uint64_t* full = sm.full[wid];
+  const long long tile_bytes = (long long)a.S * RB;
 
-  if (wid == GV_CONS_WARPS) {
-    // ------------------------------------------------------------ producer
+  // ---- producer side (lane 0 issues the copies, every lane keeps the cursor)
+  Cursor pc;
+  pc.item = gw;
+  cursor_load<MODE>(pc, a, tab, sm.act, total, g);
+  uint32_t issued = 0;
+  auto issue = [&]() {
+    if (pc.item >= total) return;
+    const int st = issued % GW_NS;
     if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int unit = u_begin; unit < u_end && ok; ++unit) {
-        const UnitInfo u = unit_info<MODE>(a, sm.act, unit);
-        const uint8_t* wexp = tab.get(u.e, a);
-        const uint8_t* b0 = wexp + (long long)u.tile0 * a.S * RB;
-        const uint8_t* b1 = wexp + (long long)u.tile1 * a.S * RB;
-        const int rounds = (u.n_e + 7) / 8;
-        for (int r = 0; r < rounds && ok; ++r) {
-          for (int c = 0; c < nchunk; ++c, ++it) {
-            const int st = it % GV_NSTAGE;
-            const uint32_t ph = (it / GV_NSTAGE) & 1u;
-            if (!mbar_wait(&sm.empty[st], ph ^ 1u, a.status)) { ok = false; break; }
-            const int ns = min(GV_CH, a.S - c * GV_CH);
-            const uint32_t wbytes = (uint32_t)(ns * RB);
-            mbar_arrive_expect_tx(&sm.full[st], 2 * wbytes);
-            bulk_g2s_stream(&sm.stage[st][0], b0 + (long long)c * GV_CH * RB, wbytes, &sm.full[st], pol);
-            bulk_g2s_stream(&sm.stage[st][GV_CH * RB], b1 + (long long)c * GV_CH * RB, wbytes, &sm.full[st], pol);
-          }
-        }
-      }
-      // drain: do not leave the CTA with copies in flight
-      for (uint32_t j = (it > GV_NSTAGE ? it - GV_NSTAGE : 0); j < it; ++j)
-        mbar_wait(&sm.full[j % GV_NSTAGE], (j / GV_NSTAGE) & 1u, a.status);
+      const int ns = min(GW_SL, pc.s1 - pc.sp);
+      const uint32_t bytes = (uint32_t)(ns * RB);
+      mbar_arrive_expect_tx(&full[st], 2 * bytes);
+      bulk_g2s(&stage[st][0], pc.w0 + pc.tile0 * tile_bytes + (long long)pc.sp * RB, bytes, &full[st]);
+      bulk_g2s(&stage[st][GW_SL * RB], pc.w1 + pc.tile1 * tile_bytes + (long long)pc.sp * RB, bytes,
+               &full[st]);
     }
-    return;
-  }
+    ++issued;
+    cursor_next<MODE>(pc, a, tab, sm.act, total, nwarps, g);
+  };
+  for (int i = 0; i < GW_NS; ++i) issue();
 
-  // -------------------------------------------------------------- consumers
   if (MODE == 1) pdl_wait();  // h comes from the gate/up kernel
-  const int g = lane >> 2, c4 = lane & 3;
-  // flat walk over (unit, round, chunk); the token fragment of the next step is loaded
-  // into registers before waiting for the current step's weights
-  int unit = u_begin, r = 0, c = 0;
-  UnitInfo u;
-  if (unit < u_end) u = unit_info<MODE>(a, sm.act, unit);
-  auto load_b = [&](const UnitInfo& uu, int rr_, int cc, uint2 (&bv)[4]) {
-    const int s = cc * GV_CH + wid;
-    if (s >= a.S) return;
-    const int rr = min(8 * rr_ + g, uu.n_e - 1);  // padded lanes re-read a valid row
-    long long row;
-    if (MODE == 0) row = a.sorted_pair ? a.sorted_pair[uu.r0 + rr] / a.k : (uu.r0 + rr);
-    else row = uu.r0 + rr;
-    const uint2* src = reinterpret_cast<const uint2*>(a.act + row * a.act_ld + s * 64 + 4 * c4);
-    const bool half = ragged && s == a.S - 1;
+
+  // ---- consumer side
+  Cursor cc;
+  cc.item = gw;
+  cursor_load<MODE>(cc, a, tab, sm.act, total, g);
+  auto load_b = [&](const Cursor& c, uint2 (&bv)[GW_SL][4]) {
+    if (c.item >= total) return;
+    const uint2* base = reinterpret_cast<const uint2*>(c.brow + 4 * c4);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j >= 2 && half) break;
-      bv[j] = MODE == 0 ? __ldg(src + 4 * j) : __ldcg(src + 4 * j);
+    for (int sl = 0; sl < GW_SL; ++sl) {
+      const int s = c.sp + sl;
+      if (s >= c.s1) break;
+      const bool half = ragged && s == a.S - 1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j >= 2 && half) break;
+        const uint2* src = base + s * 16 + 4 * j;
+        bv[sl][j] = MODE == 0 ? __ldg(src) : __ldcg(src);
+      }
     }
   };
-  uint2 bnext[4] = {};
-  if (unit < u_end) load_b(u, 0, 0, bnext);
-  uint32_t it = 0;
-  int ep = 0;  // epilogue count (red buffer parity)
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  while (unit < u_end) {
-    const uint2 bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
-    // next position
-    int nunit = unit, nr = r, nc = c + 1;
-    const int rounds = (u.n_e + 7) / 8;
-    if (nc == nchunk) {
-      nc = 0;
-      if (++nr == rounds) { nr = 0; ++nunit; }
-    }
-    UnitInfo nu = u;
-    if (nunit != unit && nunit < u_end) nu = unit_info<MODE>(a, sm.act, nunit);
-    if (nunit < u_end) load_b(nu, nr, nc, bnext);
+  uint2 bnext[GW_SL][4];
+  load_b(cc, bnext);
+  uint32_t consumed = 0;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // current part
+  float tot[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // finished parts, in order
+  while (cc.item < total) {
+    uint2 bv[GW_SL][4];
+#pragma unroll
+    for (int sl = 0; sl < GW_SL; ++sl)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[sl][j] = bnext[sl][j];
+    const Cursor cur = cc;
+    const bool done = cursor_next<MODE>(cc, a, tab, sm.act, total, nwarps, g);
+    load_b(cc, bnext);
 
-    const int st = it % GV_NSTAGE;
-    const uint32_t ph = (it / GV_NSTAGE) & 1u;
-    if (!mbar_wait(&sm.full[st], ph, a.status)) return;
-    const int ns = min(GV_CH, a.S - c * GV_CH);
-    if (wid < ns) {
-      const int s = c * GV_CH + wid;
+    const int st = consumed % GW_NS;
+    if (!mbar_wait(&full[st], (consumed / GW_NS) & 1u, a.status)) return;
+    const int ns = min(GW_SL, cur.s1 - cur.sp);
+#pragma unroll
+    for (int sl = 0; sl < GW_SL; ++sl) {
+      if (sl >= ns) break;
+      const int s = cur.sp + sl;
       const bool half = ragged && s == a.S - 1;
 #pragma unroll
       for (int ti = 0; ti < 2; ++ti) {
-        const uint8_t* rec = &sm.stage[st][(ti * GV_CH + wid) * RB];
+        const uint8_t* rec = &stage[st][(ti * GW_SL + sl) * RB];
         const uint4 q = *reinterpret_cast<const uint4*>(rec + lane * 16);
         float sc[2][2];
         load_scales<QT>(rec, g, sc);
@@ -262,7 +287,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) gemv_ffn_kernel(const GemvArgs 
           for (int jj = 0; jj < 2; ++jj) {
             uint32_t av[4];
             decode_word<QT>(wj[2 * b + jj], av);
-            mma_16816(part, av, bv[2 * b + jj].x, bv[2 * b + jj].y);
+            mma_16816(part, av, bv[sl][2 * b + jj].x, bv[sl][2 * b + jj].y);
           }
           acc[ti][0] = fmaf(sc[b][0], part[0], acc[ti][0]);
           acc[ti][1] = fmaf(sc[b][0], part[1], acc[ti][1]);
@@ -271,51 +296,83 @@ __global__ void __launch_bounds__(GV_THREADS, 1) gemv_ffn_kernel(const GemvArgs 
         }
       }
     }
+    ++consumed;
+    // the stage is free again: order this warp's reads before the next bulk write into it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[st]);
-    ++it;
+    issue();
 
-    if (nc == 0) {
-      // ---- end of (unit, round): add the 16 slab partial sums of each tile
-      const int tok0 = 8 * r;
-      float (*red)[2][4][32] = sm.red[ep & 1];
+    const int send = cur.sp + ns;
+    if (send % GW_PS == 0 || send == cur.s1) {
+      // ---- end of a fixed part
+      if (a.kp == 1) {
+#pragma unroll
+        for (int ti = 0; ti < 2; ++ti)
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) tot[ti][qq] += acc[ti][qq];
+      } else {
+        const int part = (send - 1) / GW_PS;
+        float* pb = a.partials + ((long long)cur.unit * a.NP + part) * 256;
+#pragma unroll
+        for (int ti = 0; ti < 2; ++ti)
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) __stcg(pb + (ti * 4 + qq) * 32 + lane, acc[ti][qq]);
+      }
 #pragma unroll
       for (int ti = 0; ti < 2; ++ti)
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          red[wid][ti][qq][lane] = acc[ti][qq];
-          acc[ti][qq] = 0.f;
-        }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.ebar);
-      if (!mbar_wait(&sm.ebar, ep & 1, a.status)) return;
-      if (wid < 4) {
-        const int qq = wid;
-        float v0 = 0.f, v1 = 0.f;
+        for (int qq = 0; qq < 4; ++qq) acc[ti][qq] = 0.f;
+    }
+
+    if (done) {
+      // ---- end of (item, round)
+      bool finalize = true;
+      if (a.kp > 1) {
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(&a.counters[cur.unit], 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        finalize = old == a.kp - 1;
+        if (finalize) {
+          __threadfence();
+          const float* ub = a.partials + (long long)cur.unit * a.NP * 256;
 #pragma unroll
-        for (int w2 = 0; w2 < GV_CONS_WARPS; ++w2) {
-          v0 += red[w2][0][qq][lane];
-          v1 += red[w2][1][qq][lane];
+          for (int ti = 0; ti < 2; ++ti)
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              float v = 0.f;
+              for (int p2 = 0; p2 < a.NP; ++p2) v += __ldcg(ub + p2 * 256 + (ti * 4 + qq) * 32 + lane);
+              tot[ti][qq] = v;
+            }
         }
-        const int rr = tok0 + 2 * c4 + (qq & 1);
-        if (rr < u.n_e) {
+      }
+      if (finalize) {
+        const int tok0 = 8 * cur.r;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int rr = tok0 + 2 * c4 + (qq & 1);
+          if (rr >= cur.n_e) continue;
           const int rofs = g + 8 * (qq >> 1);
-          uint16_t* orow = a.out + (long long)(u.r0 + rr) * a.out_ld;
+          uint16_t* orow = a.out + (long long)(cur.r0 + rr) * a.out_ld;
           if (MODE == 0) {
-            orow[u.tile0 * 16 + rofs] = f32_to_bf16_bits(silu_f32(v0) * v1);
+            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(silu_f32(tot[0][qq]) * tot[1][qq]);
           } else {
-            orow[u.tile0 * 16 + rofs] = f32_to_bf16_bits(v0);
-            orow[u.tile1 * 16 + rofs] = f32_to_bf16_bits(v1);
+            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(tot[0][qq]);
+            orow[cur.tile1 * 16 + rofs] = f32_to_bf16_bits(tot[1][qq]);
           }
         }
       }
-      ++ep;
+#pragma unroll
+      for (int ti = 0; ti < 2; ++ti)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) tot[ti][qq] = 0.f;
     }
-    unit = nunit;
-    r = nr;
-    c = nc;
-    u = nu;
   }
+}
+
+__global__ void zero_ints_kernel(int* p, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
 }
 
 template <class K, class... Args>
@@ -334,26 +391,72 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Part groups per unit: only for batches of at most 8 tokens (one round per expert),
+// enough groups to give every warp of the GPU about two items.
+static int pick_kp(int T, long long units, int NP, int sm_count) {
+  if (T > 8) return 1;
+  const long long want = 2LL * sm_count * 2 * GW_WARPS;
+  int kp = 1;
+  while (kp < GW_KPMAX && units * kp < want && 2 * kp <= NP) kp *= 2;
+  return kp;
+}
+
+struct GemvLayout {
+  long long u1, u2;  // units of the gate/up and down projections (upper bound)
+  int np1, np2;
+  size_t zero_bytes, total;
+  size_t off_cnt1, off_cnt2, off_p1, off_p2;
+};
+
+static GemvLayout gemv_layout(int T, int k, int E, int H, int I) {
+  GemvLayout L{};
+  if (T > 8) return L;
+  const long long mact = (long long)T * k < E ? (long long)T * k : E;
+  L.u1 = mact * (I / 16);
+  L.u2 = mact * (H / 32);
+  L.np1 = (slabs_of(H) + GW_PS - 1) / GW_PS;
+  L.np2 = (slabs_of(I) + GW_PS - 1) / GW_PS;
+  L.off_cnt1 = 0;
+  L.off_cnt2 = al256(L.u1 * 4);
+  L.zero_bytes = L.off_cnt2 + al256(L.u2 * 4);
+  L.off_p1 = L.zero_bytes;
+  L.off_p2 = L.off_p1 + al256(L.u1 * L.np1 * 1024);
+  L.total = L.off_p2 + al256(L.u2 * L.np2 * 1024);
+  return L;
+}
+
+size_t ffn_gemv_ws_bytes(int T, int k, int E, int H, int I) { return gemv_layout(T, k, E, H, I).total; }
+size_t ffn_gemv_zero_bytes(int T, int k, int E, int H, int I) {
+  return gemv_layout(T, k, E, H, I).zero_bytes;
+}
+
 template <int QT, int MODE, class Tab>
 static cudaError_t launch_mode(const GemvArgs& a, const Tab& tab, int max_active, cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   auto kern = gemv_ffn_kernel<QT, MODE, Tab>;
-  const size_t smem = sizeof(GvSmem<QT>);
+  const size_t smem = sizeof(GwSmem<QT>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  int grid = di->sm_count;
-  const int upper = max_active * a.units_per_expert;
-  if (upper < grid) grid = upper;
+  const long long items = (long long)max_active * a.units_per_expert * a.kp;
+  long long grid = (items + GW_WARPS - 1) / GW_WARPS;
+  const long long cap = (long long)di->sm_count * 2;
+  if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch_pdl(kern, dim3(grid), dim3(GV_THREADS), smem, st, a, tab);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(GW_THREADS), smem, st, a, tab);
 }
 
 template <int QT, class Tab>
-static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t st) {
+static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, bool ws_zeroed,
+                             cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   const int max_active = pb.P < pb.E ? pb.P : pb.E;
+  const GemvLayout Lw = gemv_layout(pb.T, pb.k, pb.E, pb.H, pb.I);
+  char* w = (char*)ws;
+
   GemvArgs a{};
   a.offsets = pb.offsets;
   a.sorted_pair = pb.sorted_pair;
@@ -370,33 +473,53 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t 
   a.table_off = 0;
   a.S = slabs_of(pb.H);
   a.K = pb.H;
+  a.NP = (a.S + GW_PS - 1) / GW_PS;
   a.up_rt = pb.I / 16;
   a.units_per_expert = pb.I / 16;
+  a.kp = pick_kp(pb.T, (long long)max_active * a.units_per_expert, a.NP, di->sm_count);
+  // down
+  GemvArgs d = a;
+  d.act = pb.h_act;
+  d.act_ld = pb.I;
+  d.out = pb.y_perm;
+  d.out_ld = pb.H;
+  d.wbase = pb.w2;
+  d.wstride = (long long)tiles_bytes_per_expert(pb.qtype, pb.H, pb.I);
+  d.table_off = (long long)pb.w13_bytes;
+  d.S = slabs_of(pb.I);
+  d.K = pb.I;
+  d.NP = (d.S + GW_PS - 1) / GW_PS;
+  d.up_rt = 0;
+  d.units_per_expert = pb.H / 32;
+  d.kp = pick_kp(pb.T, (long long)max_active * d.units_per_expert, d.NP, di->sm_count);
+  if (a.kp > 1 || d.kp > 1) {
+    if (!ws || Lw.total == 0) return cudaErrorInvalidValue;
+    a.counters = (int*)(w + Lw.off_cnt1);
+    a.partials = (float*)(w + Lw.off_p1);
+    d.counters = (int*)(w + Lw.off_cnt2);
+    d.partials = (float*)(w + Lw.off_p2);
+    if (!ws_zeroed) {
+      const int n = (int)(Lw.zero_bytes / 4);
+      zero_ints_kernel<<<(n + 255) / 256, 256, 0, st>>>((int*)w, n);
+      cudaError_t e0 = cudaGetLastError();
+      if (e0 != cudaSuccess) return e0;
+    }
+  }
   cudaError_t err = launch_mode<QT, 0>(a, tab, max_active, st);
   if (err != cudaSuccess) return err;
-  // down
-  a.act = pb.h_act;
-  a.act_ld = pb.I;
-  a.out = pb.y_perm;
-  a.out_ld = pb.H;
-  a.wbase = pb.w2;
-  a.wstride = (long long)tiles_bytes_per_expert(pb.qtype, pb.H, pb.I);
-  a.table_off = (long long)pb.w13_bytes;
-  a.S = slabs_of(pb.I);
-  a.K = pb.I;
-  a.up_rt = 0;
-  a.units_per_expert = pb.H / 32;
-  return launch_mode<QT, 1>(a, tab, max_active, st);
+  return launch_mode<QT, 1>(d, tab, max_active, st);
 }
 
-cudaError_t launch_ffn_gemv(const FfnProblem& pb, cudaStream_t st) {
+cudaError_t launch_ffn_gemv(const FfnProblem& pb, void* ws, bool ws_zeroed, cudaStream_t st) {
   if (pb.table) {
     WithTable t;
     t.t = *pb.table;
-    return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, st) : launch_qt<FTMOE_MXFP4>(pb, t, st);
+    return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
+                                  : launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st);
   }
   NoTable t;
-  return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, st) : launch_qt<FTMOE_MXFP4>(pb, t, st);
+  return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
+                                : launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st);
 }
 
 }  // namespace ftmoe

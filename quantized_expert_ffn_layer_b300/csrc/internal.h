@@ -25,9 +25,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
                          cudaStream_t st);
 
 size_t permute_ws_bytes(int T, int k, int E);
+// Also zeroes zero_bytes (a multiple of 4) at zero_ptr when zero_ptr is not null.
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, void* ws, int* status,
-                           cudaStream_t st);
+                           void* zero_ptr, size_t zero_bytes, cudaStream_t st);
 
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_pos,
                            const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
@@ -54,7 +55,11 @@ struct FfnProblem {
   int P;                      // T * k
 };
 
-cudaError_t launch_ffn_gemv(const FfnProblem& pb, cudaStream_t st);
+// ws: ffn_gemv_ws_bytes of scratch whose first ffn_gemv_zero_bytes must be zero on entry;
+// ws_zeroed tells that the caller already cleared them (otherwise a kernel does).
+cudaError_t launch_ffn_gemv(const FfnProblem& pb, void* ws, bool ws_zeroed, cudaStream_t st);
+size_t ffn_gemv_ws_bytes(int T, int k, int E, int H, int I);
+size_t ffn_gemv_zero_bytes(int T, int k, int E, int H, int I);
 // Grouped GEMM on tcgen05; returns cudaErrorNotSupported when the shape is outside
 // what the kernel handles (callers then use the GEMV path).
 cudaError_t launch_ffn_gemm(const FfnProblem& pb, void* ws, size_t ws_bytes, cudaStream_t st);

@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(PCHUNK) permute_small_kernel(const int32_t* __
                                                               int E, int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ sorted_pair,
                                                               int32_t* __restrict__ inv_pos,
-                                                              int* status) {
+                                                              int* status, int* zero_ptr, int zero_n) {
   extern __shared__ int sm[];
+  for (int i = threadIdx.x; i < zero_n; i += PCHUNK) zero_ptr[i] = 0;
   int* wcnt = sm;                 // [32][E]
   int* cnt = wcnt + 32 * E;       // [E]
   int* base = cnt + E;            // [E]
@@ -131,8 +132,10 @@ __global__ void __launch_bounds__(PCHUNK) permute_small_kernel(const int32_t* __
 // Large P, step 1: per-chunk histogram hist[c][E].
 __global__ void __launch_bounds__(PCHUNK) permute_count_kernel(const int32_t* __restrict__ ids, int P,
                                                               int E, int32_t* __restrict__ hist,
-                                                              int* status) {
+                                                              int* status, int* zero_ptr, int zero_n) {
   extern __shared__ int cnt[];
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_n; i += PCHUNK) zero_ptr[i] = 0;
   for (int x = threadIdx.x; x < E; x += PCHUNK) cnt[x] = 0;
   __syncthreads();
   const int e = load_id(ids, (long long)blockIdx.x * PCHUNK + threadIdx.x, P, E, status);
@@ -197,19 +200,22 @@ size_t permute_ws_bytes(int T, int k, int E) {
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, void* ws, int* status,
-                           cudaStream_t st) {
+                           void* zero_ptr, size_t zero_bytes, cudaStream_t st) {
   const int P = T * k;
+  const int zero_n = zero_ptr ? (int)(zero_bytes / 4) : 0;
   if (P <= PSMALL_MAX) {
     const size_t smem = (size_t)(35 * E + 32) * sizeof(int);
     cudaError_t err = cudaFuncSetAttribute(permute_small_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    permute_small_kernel<<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status);
+    permute_small_kernel<<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status,
+                                                (int*)zero_ptr, zero_n);
     return cudaGetLastError();
   }
   const int nchunk = (P + PCHUNK - 1) / PCHUNK;
   int32_t* hist = (int32_t*)ws;
-  permute_count_kernel<<<nchunk, PCHUNK, E * sizeof(int), st>>>(ids, P, E, hist, status);
+  permute_count_kernel<<<nchunk, PCHUNK, E * sizeof(int), st>>>(ids, P, E, hist, status,
+                                                               (int*)zero_ptr, zero_n);
   permute_scan_kernel<<<1, PCHUNK, 0, st>>>(hist, nchunk, E, offsets);
   const size_t smem = (size_t)33 * E * sizeof(int);
   cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,

@@ -87,6 +87,35 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
 
 
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "expert_ffn_gemv": ["gemv.cu", "common.cuh", "pipeline.cuh"],
+}
+
+
+def kernel_src_hash(kernel: str) -> str:
+    """sha256 over the sources of one kernel (to tell whether recorded counters still apply)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "quantized_expert_ffn_layer_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM read+write bytes per launch from a committed ncu capture, or None when the
+    capture was of another workload or the kernel's sources changed since."""
+    try:
+        with open(TRAFFIC) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("workload") != workload or rec.get("src_sha") != kernel_src_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def unique_experts(ids: np.ndarray) -> int:
     return int(len(np.unique(ids)))
 
@@ -256,7 +285,8 @@ def main():
     achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "expert FFN (gate/up+SwiGLU GEMV, down GEMV)",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_kind": f"{pk_kind} hbm_gbs (copy)", "traffic": None,
+                "peak_kind": f"{pk_kind} hbm_gbs (copy)",
+                "traffic": recorded_traffic("expert_ffn_gemv", cfg["workload"]),
                 "alg_bytes_per_launch": alg_bytes, "ms_per_launch": ffn_ms, "unique_experts": U}
     layer_bytes = alg_bytes + T * E * 4
     layer_frac = layer_bytes / (np.mean(step_ms) / 1e3) / 1e9 / hbm

@@ -137,6 +137,24 @@ ftmoe_status ftmoe_permute(const int32_t* ids, int T, int k, int E, int32_t* off
                            int32_t* sorted_pair, int32_t* inv_pos, void* ws, size_t ws_bytes,
                            ftmoe_stream_t stream);
 
+/* Same result as ftmoe_permute, for callers that can neither call cudaMalloc nor
+ * pass a workspace: a host program that owns all device memory through its own
+ * fixed pool, or a plugin interface with no workspace hook.  It allocates nothing;
+ * the scratch lives in a fixed 1 MiB device array inside the library (held on every
+ * device that loads the library until the process exits).  The pages have no
+ * counterpart to this call; it exists only for such callers.
+ *   Limit: when T * k > 16384 the call needs ceil(T * k / 1024) * E int32 of
+ *   scratch, at most 262144 (e.g. T * k <= 2,097,152 at E = 128); larger problems
+ *   return FTMOE_ERR_WORKSPACE and enqueue nothing.
+ *   Set-up: the first call on each device resolves the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before
+ *   any stream capture.
+ *   Sharing: every call on a device uses the same array, and nothing in it needs to
+ *   start at zero.  Calls whose kernels overlap on the GPU (different streams with
+ *   no ordering between them) race on the array and give undefined results. */
+ftmoe_status ftmoe_permute_noalloc(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                                   int32_t* sorted_pair, int32_t* inv_pos, ftmoe_stream_t stream);
+
 /* ------------------------------------------------------------------ expert FFN
  * [P5] §五 ExpertFFN: for every expert e and every row r in
  * [offsets[e], offsets[e+1]) with token t = sorted_pair[r] / k:

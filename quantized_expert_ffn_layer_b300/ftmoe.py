@@ -67,6 +67,7 @@ _SIGS = {
     "ftmoe_route": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "ftmoe_permute_workspace_bytes": (_sz, [_i, _i, _i]),
     "ftmoe_permute": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "ftmoe_permute_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "ftmoe_expert_blob_bytes": (_sz, [_i, _i, _i]),
     "ftmoe_ffn_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "ftmoe_layer_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -145,6 +146,12 @@ def ftmoe_permute_workspace_bytes(T, k, E):
 def ftmoe_permute(ids, T, k, E, offsets, sorted_pair, inv_pos, ws, ws_bytes, stream=None):
     _check("ftmoe_permute", lib.ftmoe_permute(_p(ids), T, k, E, _p(offsets), _p(sorted_pair),
                                               _p(inv_pos), _p(ws), ws_bytes, _s(stream)))
+
+
+def ftmoe_permute_noalloc(ids, T, k, E, offsets, sorted_pair, inv_pos, stream=None):
+    _check("ftmoe_permute_noalloc", lib.ftmoe_permute_noalloc(_p(ids), T, k, E, _p(offsets),
+                                                              _p(sorted_pair), _p(inv_pos),
+                                                              _s(stream)))
 
 
 def ftmoe_expert_blob_bytes(qtype, H, I):

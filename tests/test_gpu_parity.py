@@ -256,3 +256,68 @@ def test_prefill_layer_sampled_parity(env, qtype):
     rids, _, rout = oracle.layer_rows(L.x, L.logits, L.k, L.qtype, L.w13, L.w2, rows)
     assert np.array_equal(ids[rows], rids)
     assert rel_l2(out[rows], rout) <= LAYER_TOL
+
+
+# ------------------------------------------------------------------ tensor-core grouped GEMM
+@pytest.mark.parametrize("qtype", ["q4_0", "mxfp4"])
+@pytest.mark.parametrize("T", [64, 300])
+def test_gemm_path_decode_shape_full_parity(env, qtype, T):
+    """The tcgen05 path on the decode layer shape: few rows per expert (narrow MMA N)."""
+    c = dict(CONFIGS["decode"])
+    c.update(T=T, qtype=qtype)
+    L = make_layer(**c)
+    _, out, ids, _ = _layer_gpu(env, L, path=2)
+    r = oracle.layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2)
+    assert np.array_equal(ids, r["ids"])
+    assert rel_l2(out, r["out"]) <= LAYER_TOL
+
+
+@pytest.mark.parametrize("qtype", ["q4_0", "mxfp4"])
+def test_gemm_path_several_token_tiles_per_expert(env, qtype):
+    """Experts with 300-400 rows: two 256-row token tiles each, the second one ragged."""
+    L = make_layer(H=256, I=128, E=4, k=2, T=700, qtype=qtype, seed=4, zipf=0.5)
+    _, out, ids, _ = _layer_gpu(env, L, path=2)
+    r = oracle.layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2)
+    assert np.array_equal(ids, r["ids"])
+    assert rel_l2(out, r["out"]) <= LAYER_TOL
+    # per-row check too: every row of the output within tolerance, not only on average
+    num = np.linalg.norm(out - r["out"], axis=1)
+    den = np.linalg.norm(r["out"], axis=1)
+    assert np.all(num <= 2e-2 * den)
+
+
+def test_gemm_path_ragged_shapes_and_shared_expert(env):
+    """H = 224, I = 96: partial 128-row weight tiles and a half-filled last reduction block."""
+    L = make_layer(H=224, I=96, E=5, k=3, T=300, qtype="mxfp4", seed=9, shared=True)
+    _, out, ids, _ = _layer_gpu(env, L, path=2)
+    r = oracle.layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2, L.shared_w13, L.shared_w2)
+    assert np.array_equal(ids, r["ids"])
+    assert rel_l2(out, r["out"]) <= LAYER_TOL
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_expert_blob_table_matches_contiguous_weights(env, path):
+    """Weights reached through a per-expert pointer table (cache slots) give the same bits."""
+    F, torch, dev = env
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    L = make_layer(H=256, I=128, E=8, k=2, T=200, qtype="q4_0", seed=21)
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, device=dev)
+    blobs = torch.cat([m.w13.view(L.E, -1), m.w2.view(L.E, -1)], dim=1).contiguous()
+    nb = blobs.shape[1]
+    assert nb == F.ftmoe_expert_blob_bytes(L.qtype, L.H, L.I)
+    # reverse the slot order so that the table is not the identity layout
+    slots = torch.flip(blobs, dims=[0]).contiguous()
+    ptrs = [slots.data_ptr() + (L.E - 1 - e) * nb for e in range(L.E)]
+    wt = F.make_weights(L.qtype, L.E, L.H, L.I, expert_blob=ptrs)
+    lg = torch.from_numpy(L.logits).to(dev)
+    x = bf16_tensor(L.x, dev)
+    old = F.ftmoe_set_ffn_path(path)
+    try:
+        ref = m.forward(lg, x, L.k)
+        ws = m.workspace(L.T, L.k)
+        out = torch.empty_like(ref)
+        F.ftmoe_layer(wt, lg, x, L.T, L.k, out, None, None, ws, ws.numel())
+        torch.cuda.synchronize()
+    finally:
+        F.ftmoe_set_ffn_path(old)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

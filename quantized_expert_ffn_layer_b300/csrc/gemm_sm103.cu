@@ -6,21 +6,28 @@
 // One persistent CTA per SM.  A work item is (expert, 128 feature rows x 2 tiles,
 // up to 256 of the expert's token rows): for gate/up the two tiles are the gate and
 // the up rows of the same 128 features, for down two consecutive 128-row tiles of
-// the output.  Per 64-element reduction block:
-//   * 8 producer warps decode the 4-bit weight records straight from HBM into exact
-//     bf16 (round-to-nearest-even of the decoded value) and gather the token rows,
-//     writing both into the 128-byte-swizzled K-major shared-memory layout that
-//     the MMA descriptors read (3-stage ring, mbarrier full/empty);
+// the output.  Per 64-element reduction block ("stage"):
+//   * a loader warp copies the stage's 16 raw weight records (16 rows x 64 codes +
+//     scales each) into a ring of shared-memory slots with 1-D bulk copies, and the
+//     token rows into the 128-byte-swizzled K-major B tile with TMA tensor loads
+//     (one 64 x 256 box for the down projection, whose rows are contiguous; one
+//     64 x 1 box per row for gate/up, whose rows are gathered by the permutation);
+//   * 8 converter warps decode the raw records into exact bf16 (round-to-nearest-
+//     even of the decoded value) in the swizzled K-major A tiles;
 //   * one thread issues tcgen05.mma kind::f16 (M = 128 weight rows, N = the token
 //     count rounded up to 16, K = 16) into two fp32 accumulators in tensor memory
-//     (columns [0, 256) and [256, 512)) and commits each stage back to the
-//     producers;
+//     (columns [0, 256) and [256, 512)) and commits each stage back to the ring;
 //   * 4 epilogue warps read the accumulators with tcgen05.ld and write
 //     h = silu(gate) * up (gate/up) or y (down) as bf16.
 // The weights are the A operand (M) and the tokens the B operand (N), so a small
 // expert costs a narrow MMA rather than a mostly empty 128-row tile.  Items are
 // ordered expert by expert with the token tile innermost, so CTAs that run at the
 // same time share weight tiles through L2.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -30,33 +37,38 @@ namespace ftmoe {
 
 constexpr int GM_TOK = 256;         // token rows per item (largest MMA N)
 constexpr int GM_ROWS = 128;        // weight rows per tile (MMA M)
-constexpr int GM_NS = 3;            // pipeline stages
+constexpr int GM_NS = 3;            // A/B operand stages
+constexpr int GM_NR = 3;            // raw weight stages
 constexpr int GM_EPI_WARPS = 4;     // warps 0..3 (one per TMEM lane quarter)
 constexpr int GM_MMA_WARP = 4;      // TMEM owner; lane 0 issues the MMAs
-constexpr int GM_PROD0 = 5;         // first producer warp
-constexpr int GM_PROD_WARPS = 8;
-constexpr int GM_PROD_THREADS = GM_PROD_WARPS * 32;
-constexpr int GM_THREADS = (GM_PROD0 + GM_PROD_WARPS) * 32;  // 416
+constexpr int GM_RAW_WARP = 5;      // bulk copies of the raw weight records
+constexpr int GM_TOK_WARP = 6;      // token rows: TMA box (down) or cp.async gather (gate/up)
+constexpr int GM_CONV0 = 7;         // first converter warp
+constexpr int GM_CONV_WARPS = 8;
+constexpr int GM_THREADS = (GM_CONV0 + GM_CONV_WARPS) * 32;  // 480
 constexpr uint32_t GM_TMEM_COLS = 512;
 constexpr int GM_A_TILE = GM_ROWS * 128;           // 16 KB of bf16 (128 rows x 64)
 constexpr int GM_B_TILE = GM_TOK * 128;            // 32 KB of bf16 (256 rows x 64)
 constexpr int GM_STAGE = 2 * GM_A_TILE + GM_B_TILE;
+constexpr int GM_RAW_STAGE = 16 * 576;             // 16 records (Q4_0 size; MXFP4 uses less)
 constexpr int GM_MAX_E = 1024;
 
 struct GemmTail {
-  uint64_t full[GM_NS], empty[GM_NS];
+  uint64_t a_full[GM_NS], b_full[GM_NS], empty[GM_NS];
+  uint64_t raw_full[GM_NR], raw_empty[GM_NR];
   uint64_t acc_full, acc_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
   int citem[GM_MAX_E + 1];  // exclusive prefix of items per expert
 };
-constexpr size_t GM_SMEM = 1024 + (size_t)GM_NS * GM_STAGE + sizeof(GemmTail);
+constexpr size_t GM_SMEM =
+    1024 + (size_t)GM_NS * GM_STAGE + (size_t)GM_NR * GM_RAW_STAGE + sizeof(GemmTail);
 
 struct GemmArgs {
   const int32_t* offsets;
   const int32_t* sorted_pair;  // gate/up: pair of each permuted row (nullptr: identity)
   int k, E;
-  const uint16_t* act;  // gate/up: x [T][H]; down: h [P][I]
+  const uint16_t* act;  // gate/up: x [T][H] (rows gathered); down: h [P][I] (via act_map)
   int act_ld;
   uint16_t* out;        // gate/up: h [P][I]; down: y_perm [P][H]
   int out_ld;
@@ -106,6 +118,22 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   return it;
 }
 
+// First matrix row of record ri (tile ri / 8, 16-row group ri % 8) of an item, and
+// whether that row group lies inside the projection's result rows.
+template <int MODE>
+__device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const GemmArgs& a,
+                                             bool& ok) {
+  const int t = ri >> 3, rg = ri & 7;
+  if (MODE == 0) {
+    const int row = it.f0 + rg * 16;
+    ok = row < a.nrows;
+    return t ? row + a.up_row0 : row;
+  }
+  const int row = it.f0 + t * GM_ROWS + rg * 16;
+  ok = row < a.nrows;
+  return row;
+}
+
 // ---------------------------------------------------------------- weight decode
 // W holds 8 four-bit codes of one row as nibble slots (0,4,2,6,1,5,3,7) = elements
 // 0..7; slots p and p + 4 form the bf16x2 pair p.  Returns the 8 bf16 in element
@@ -151,18 +179,19 @@ __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
   return b | (b << 16);
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
 }
 
 // Permutes the four words so that w[s] becomes the old w[s ^ h] (h = 0..3).
@@ -177,163 +206,111 @@ __device__ __forceinline__ void xperm4(uint32_t (&w)[4], int h) {
   }
 }
 
-// Per producer thread and stage: its share of one weight record (the 32 code bytes of
-// lanes 4g + 2m and 4g + 2m + 1, i.e. 8 elements x 4 words of rows g and g + 8) plus
-// the scales of those rows, and 8 token-row chunks of 16 bytes.
-struct ProdData {
-  uint4 ca, cb;
-  uint2 sc;
-  uint4 b[8];
-  int rec_ok;      // the record lies inside the matrix
-  uint32_t bmask;  // bit i: token chunk i exists
-};
-
-// Where the producer thread loads from for the stage (item, kb).
-struct ProdCtx {
-  int item, kb;
-  int rec_ok;
-  const uint8_t* rec0;  // this thread's record at kb = 0 (advance by kb * RB)
-  int arow[8];          // act rows of this thread's 8 token chunks (-1: none)
-};
-
-template <int QT, int MODE, class Tab>
-__device__ __forceinline__ void prod_ctx_item(ProdCtx& c, int item, const GemmArgs& a,
-                                              const Tab& tab, const int* citem, int pt) {
-  const GmItem it = gm_item<MODE>(item, a, citem);
-  c.item = item;
-  c.kb = 0;
-  const int lane = pt & 31, pw = pt >> 5;
-  const int ri = pw * 2 + (lane >> 4);  // record of the stage: tile ri / 8, row group ri % 8
-  const int t = ri >> 3, rg = ri & 7;
-  int row;  // first row of the 16-row group within the matrix
-  if (MODE == 0) {
-    row = it.f0 + rg * 16;
-    c.rec_ok = row < a.nrows;
-    if (t == 1) row += a.up_row0;
+// One converter thread's share of a record: the 32 code bytes of record lanes 4g + 2m
+// and 4g + 2m + 1 (elements 8m..8m+7 of each 16-element step of rows g and g + 8),
+// decoded into rows rg*16 + g and rg*16 + g + 8 of the A tile.
+template <int QT>
+__device__ __forceinline__ void convert_record(uint32_t rec, uint32_t tile, int rg, int g, int m) {
+  const uint4 ca = lds128(rec + (4 * g + 2 * m) * 16);
+  const uint4 cb = lds128(rec + (4 * g + 2 * m + 1) * 16);
+  uint32_t shi[2][2], slo[2][2];  // [block][row half]
+  if (QT == FTMOE_Q4_0) {
+    uint32_t s0, s1;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(s0), "=r"(s1)
+                 : "r"(rec + REC_CODE_BYTES + g * 8)
+                 : "memory");
+    split_scale(s0 & 0xFFFFu, shi[0][0], slo[0][0]);
+    split_scale(s0 >> 16, shi[0][1], slo[0][1]);
+    split_scale(s1 & 0xFFFFu, shi[1][0], slo[1][0]);
+    split_scale(s1 >> 16, shi[1][1], slo[1][1]);
   } else {
-    row = it.f0 + t * GM_ROWS + rg * 16;
-    c.rec_ok = row < a.nrows;
-  }
-  constexpr int RB = rec_bytes(QT);
-  c.rec0 = tab.get(it.e, a) + (long long)(row / 16) * a.S * RB;
+    uint32_t s0;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s0) : "r"(rec + REC_CODE_BYTES + g * 4) : "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = (pt >> 3) + 32 * i;
-    int ar = -1;
-    if (rr < it.n) {
-      if (MODE == 0) ar = a.sorted_pair ? a.sorted_pair[it.r0 + rr] / a.k : (it.r0 + rr);
-      else ar = it.r0 + rr;
-    }
-    c.arow[i] = ar;
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        shi[b][h] = e8m0_bf16x2((s0 >> (8 * (2 * b + h))) & 0xFFu);
+        slo[b][h] = 0;
+      }
+  }
+  uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+  uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
+  // step s handles word j = s ^ h(g): with the row swizzle (chunk ^ g) this puts the
+  // 8 lanes of each quarter-warp on 8 different 16-byte bank groups
+  const int hx = (((g >> 1) & 1) << 1) | ((g ^ (g >> 1)) & 1);
+  xperm4(wa, hx);
+  xperm4(wb, hx);
+  const uint32_t row0 = tile + (2 * rg) * 1024 + g * 128;  // row rg*16 + g
+  const uint32_t row1 = row0 + 1024;                       // row rg*16 + g + 8
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int j = s ^ hx;
+    const int b = j >> 1;
+    const uint32_t A = wa[s], B = wb[s];
+    const uint32_t wg = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
+    const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
+    const uint32_t sh0 = b ? shi[1][0] : shi[0][0], sl0 = b ? slo[1][0] : slo[0][0];
+    const uint32_t sh1 = b ? shi[1][1] : shi[0][1], sl1 = b ? slo[1][1] : slo[0][1];
+    const uint32_t cp = 2 * j + m;
+    const uint32_t off = ((cp ^ (uint32_t)g) * 16);
+    sts128(row0 + off, decode8<QT>(wg, sh0, sl0));
+    sts128(row1 + off, decode8<QT>(wg8, sh1, sl1));
   }
 }
 
-template <int QT>
-__device__ __forceinline__ void prod_load(const ProdCtx& c, const GemmArgs& a, int pt,
-                                          ProdData& d) {
-  constexpr int RB = rec_bytes(QT);
-  const int lane = pt & 31;
-  const int g = (lane & 15) >> 1, m = lane & 1;
-  d.rec_ok = c.rec_ok;
-  if (c.rec_ok) {
-    const uint8_t* rec = c.rec0 + (long long)c.kb * RB;
-    d.ca = ldg_stream(rec + (4 * g + 2 * m) * 16);
-    d.cb = ldg_stream(rec + (4 * g + 2 * m + 1) * 16);
-    if (QT == FTMOE_Q4_0) {
-      d.sc = __ldg(reinterpret_cast<const uint2*>(rec + REC_CODE_BYTES + g * 8));
-    } else {
-      d.sc.x = __ldg(reinterpret_cast<const uint32_t*>(rec + REC_CODE_BYTES + g * 4));
-      d.sc.y = 0;
-    }
-  }
-  const int col = c.kb * 64 + 8 * (pt & 7);
-  const bool kok = col < a.K;
-  uint32_t mask = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (c.arow[i] >= 0) {
-      mask |= 1u << i;
-      const uint16_t* p = a.act + (long long)c.arow[i] * a.act_ld + col;
-      d.b[i] = kok ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0, 0, 0, 0);
-    }
-  }
-  d.bmask = mask;
+// 16-byte global -> shared copy (LDGSTS); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int QT>
-__device__ __forceinline__ void prod_store(const ProdData& d, int pt, uint32_t stage_addr) {
-  const int lane = pt & 31, pw = pt >> 5;
-  if (d.rec_ok) {
-    const int ri = pw * 2 + (lane >> 4);
-    const int t = ri >> 3, rg = ri & 7;
-    const int g = (lane & 15) >> 1, m = lane & 1;
-    // scales of rows g (h = 0) and g + 8 (h = 1) for blocks b = 0, 1
-    uint32_t shi[2][2], slo[2][2];
-    if (QT == FTMOE_Q4_0) {
-      split_scale(d.sc.x & 0xFFFFu, shi[0][0], slo[0][0]);
-      split_scale(d.sc.x >> 16, shi[0][1], slo[0][1]);
-      split_scale(d.sc.y & 0xFFFFu, shi[1][0], slo[1][0]);
-      split_scale(d.sc.y >> 16, shi[1][1], slo[1][1]);
-    } else {
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          shi[b][h] = e8m0_bf16x2((d.sc.x >> (8 * (2 * b + h))) & 0xFFu);
-          slo[b][h] = 0;
-        }
-    }
-    uint32_t wa[4] = {d.ca.x, d.ca.y, d.ca.z, d.ca.w};
-    uint32_t wb[4] = {d.cb.x, d.cb.y, d.cb.z, d.cb.w};
-    // step s handles word j = s ^ h(g): with the row swizzle (chunk ^ g) this puts the
-    // 8 lanes of each quarter-warp on 8 different 16-byte bank groups
-    const int hx = (((g >> 1) & 1) << 1) | ((g ^ (g >> 1)) & 1);
-    xperm4(wa, hx);
-    xperm4(wb, hx);
-    const uint32_t tile = stage_addr + t * GM_A_TILE;
-    const uint32_t row0 = tile + (2 * rg) * 1024 + g * 128;  // row rg*16 + g
-    const uint32_t row1 = row0 + 1024;                       // row rg*16 + g + 8
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int j = s ^ hx;
-      const int b = j >> 1;
-      const uint32_t A = wa[s], B = wb[s];
-      const uint32_t wg = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
-      const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
-      const uint32_t sh0 = b ? shi[1][0] : shi[0][0], sl0 = b ? slo[1][0] : slo[0][0];
-      const uint32_t sh1 = b ? shi[1][1] : shi[0][1], sl1 = b ? slo[1][1] : slo[0][1];
-      const uint32_t cp = 2 * j + m;
-      const uint32_t off = ((cp ^ (uint32_t)g) * 16);
-      sts128(row0 + off, decode8<QT>(wg, sh0, sl0));
-      sts128(row1 + off, decode8<QT>(wg8, sh1, sl1));
-    }
-  }
-  const uint32_t btile = stage_addr + 2 * GM_A_TILE;
-  const int ch = pt & 7;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (d.bmask & (1u << i)) {
-      const int rr = (pt >> 3) + 32 * i;
-      sts128(btile + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16), d.b[i]);
-    }
-  }
+// Brings [p, p + bytes) into L2 ahead of use (bytes % 16 == 0, p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 2-D TMA tile load (box from the tensor map) into shared memory, completion counted
+// on `bar`.  c0 is the inner (element) coordinate, c1 the row.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
 }
 
 template <int QT, int MODE, class Tab>
-__global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs a,
-                                                               const __grid_constant__ Tab tab) {
+__global__ void __launch_bounds__(GM_THREADS, 1)
+    gemm_ffn_kernel(const GemmArgs a, const __grid_constant__ Tab tab,
+                    const __grid_constant__ CUtensorMap act_map) {
+  constexpr int RB = rec_bytes(QT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_addr - raw_addr);
-  GemmTail& tl = *reinterpret_cast<GemmTail*>(base + (size_t)GM_NS * GM_STAGE);
+  const uint32_t rawring = base_addr + GM_NS * GM_STAGE;
+  GemmTail& tl =
+      *reinterpret_cast<GemmTail*>(base + (size_t)GM_NS * GM_STAGE + (size_t)GM_NR * GM_RAW_STAGE);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &tl.abort_flag;
 
   if (tid == 0) {
     for (int s = 0; s < GM_NS; ++s) {
-      mbar_init(&tl.full[s], GM_PROD_THREADS);
+      mbar_init(&tl.a_full[s], GM_CONV_WARPS);
+      mbar_init(&tl.b_full[s], 1);
       mbar_init(&tl.empty[s], 1);
+    }
+    for (int s = 0; s < GM_NR; ++s) {
+      mbar_init(&tl.raw_full[s], 1);
+      mbar_init(&tl.raw_empty[s], GM_CONV_WARPS);
     }
     mbar_init(&tl.acc_full, 1);
     mbar_init(&tl.acc_empty, GM_EPI_WARPS * 32);
@@ -370,36 +347,112 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs 
   const int nitems = tl.citem[a.E];
   const int G = gridDim.x;
 
-  if (warp >= GM_PROD0) {
-    // ------------------------------------------------------------ producers
-    const int pt = tid - GM_PROD0 * 32;
-    ProdCtx c;
-    int slot = 0;
-    uint32_t phase = 0;
-    if (blockIdx.x < nitems) {
-      prod_ctx_item<QT, MODE>(c, blockIdx.x, a, tab, tl.citem, pt);
-      ProdData dc;
-      prod_load<QT>(c, a, pt, dc);
-      for (;;) {
-        // advance to the next stage: next block of the item, or the CTA's next item
-        bool have_next = true;
-        if (c.kb + 1 < a.S) {
-          ++c.kb;
-        } else if (c.item + G < nitems) {
-          prod_ctx_item<QT, MODE>(c, c.item + G, a, tab, tl.citem, pt);
-        } else {
-          have_next = false;
-        }
-        ProdData dn;
-        if (have_next) prod_load<QT>(c, a, pt, dn);
-        if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
-        prod_store<QT>(dc, pt, base_addr + slot * GM_STAGE);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&tl.full[slot]);
-        if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
-        if (!have_next) break;
-        dc = dn;
+  if (warp == GM_RAW_WARP) {
+    // ------------------------------------------------------------ raw weight records
+    int rslot = 0;
+    uint32_t rphase = 0;
+    for (int i = blockIdx.x; i < nitems; i += G) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      // lane r < 16: record r of every stage (tile r / 8, row group r % 8)
+      bool rok = false;
+      const uint8_t* rec0 = nullptr;
+      if (lane < 16)
+        rec0 = tab.get(it.e, a) + (long long)(gm_record_row<MODE>(it, lane, a, rok) / 16) * a.S * RB;
+      const int nrec = __popc(__ballot_sync(0xffffffffu, lane < 16 && rok));
+      // warm L2 with the CTA's next item's records while this one streams
+      if (i + G < nitems && lane < 16) {
+        const GmItem nx = gm_item<MODE>(i + G, a, tl.citem);
+        bool nok;
+        const int nrow = gm_record_row<MODE>(nx, lane, a, nok);
+        if (nok) prefetch_l2(tab.get(nx.e, a) + (long long)(nrow / 16) * a.S * RB, (uint32_t)(a.S * RB));
       }
+      for (int kb = 0; kb < a.S; ++kb) {
+        if (!mbar_wait_or_abort(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * RB));
+        __syncwarp();
+        if (lane < 16 && rok)
+          bulk_g2s(base + GM_NS * GM_STAGE + rslot * GM_RAW_STAGE + lane * RB,
+                   rec0 + (long long)kb * RB, RB, &tl.raw_full[rslot]);
+        if (++rslot == GM_NR) { rslot = 0; rphase ^= 1u; }
+      }
+      if (*abort_flag) break;
+    }
+  } else if (warp == GM_TOK_WARP) {
+    // ------------------------------------------------------------ token rows, down projection
+    // (h rows of an item are contiguous: one 64 x 256 TMA box per stage)
+    if (MODE == 1) {
+      int slot = 0;
+      uint32_t phase = 0;
+      for (int i = blockIdx.x; i < nitems; i += G) {
+        const GmItem it = gm_item<MODE>(i, a, tl.citem);
+        for (int kb = 0; kb < a.S; ++kb) {
+          if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&tl.b_full[slot], (uint32_t)GM_B_TILE);
+            tma_load_2d(base_addr + slot * GM_STAGE + 2 * GM_A_TILE, &act_map, kb * 64, it.r0,
+                        &tl.b_full[slot]);
+          }
+          if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
+        }
+        if (*abort_flag) break;
+      }
+    }
+  } else if (warp >= GM_CONV0) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - GM_CONV0 * 32;
+    const int ri = (ct >> 5) * 2 + (lane >> 4);  // record of the stage
+    const int g = (lane & 15) >> 1, m = lane & 1;
+    int slot = 0, rslot = 0;
+    uint32_t phase = 0, rphase = 0;
+    // gate/up token rows: this thread copies 16-byte chunk (ct & 7) of rows (ct >> 3) + 32 r
+    const int ch = ct & 7;
+    for (int i = blockIdx.x; i < nitems; i += G) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      bool rok;
+      gm_record_row<MODE>(it, ri, a, rok);
+      const uint16_t* rowp[8];
+      if (MODE == 0) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int rr = (ct >> 3) + 32 * r;
+          rowp[r] = nullptr;
+          if (rr < it.n) {
+            const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + rr] / a.k : (it.r0 + rr);
+            rowp[r] = a.act + ar * a.act_ld + ch * 8;
+          }
+        }
+      }
+      for (int kb = 0; kb < a.S; ++kb) {
+        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
+        if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+        const uint32_t st_addr = base_addr + slot * GM_STAGE;
+        if (MODE == 0) {
+          const uint32_t bt = st_addr + 2 * GM_A_TILE;
+          const bool kok = kb * 64 + ch * 8 < a.K;  // beyond K: zeros
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (rowp[r]) {
+              const int rr = (ct >> 3) + 32 * r;
+              cp_async16(bt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16),
+                         kok ? rowp[r] + kb * 64 : rowp[r], kok ? 16u : 0u);
+            }
+          }
+          cp_async_commit();
+        }
+        if (rok)
+          convert_record<QT>(rawring + rslot * GM_RAW_STAGE + ri * RB, st_addr + (ri >> 3) * GM_A_TILE,
+                             ri & 7, g, m);
+        if (MODE == 0) cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tl.raw_empty[rslot]);
+          mbar_arrive(&tl.a_full[slot]);
+        }
+        if (++rslot == GM_NR) { rslot = 0; rphase ^= 1u; }
+        if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
+      }
+      if (*abort_flag) break;
     }
   } else if (warp == GM_MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
@@ -414,7 +467,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs 
         if (!mbar_wait_or_abort(&tl.acc_empty, acc_phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < a.S; ++kb) {
-          if (!mbar_wait_or_abort(&tl.full[slot], phase, abort_flag, a.status)) { ok = false; break; }
+          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status) ||
+              (MODE == 1 && !mbar_wait_or_abort(&tl.b_full[slot], phase, abort_flag, a.status))) {
+            ok = false;
+            break;
+          }
           tc_fence_after_sync();
           const uint32_t sa = base_addr + slot * GM_STAGE;
 #pragma unroll
@@ -439,7 +496,6 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs 
   } else {
     // ------------------------------------------------------------ epilogue (warps 0..3)
     const int q = warp;  // TMEM lanes [32q, 32q + 32)
-    const int m = 32 * q + lane;
     uint32_t acc_phase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
@@ -447,39 +503,44 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs 
       acc_phase ^= 1u;
       tc_fence_after_sync();
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-      if (MODE == 0) {
-        const int fi = it.f0 + m;
+      // Lanes 2p and 2p + 1 swap values so that each stores two adjacent features (one
+      // bf16x2 word): the even lane for the even tokens, the odd lane for the odd ones.
+      const int odd = lane & 1;
+      const int fpair = 32 * q + (lane & ~1);  // first feature of the pair within the item
+#pragma unroll 1
+      for (int t = 0; t < (MODE == 0 ? 1 : 2); ++t) {
+        const int fi = it.f0 + t * GM_ROWS + fpair;
         const bool ok = fi < a.nrows;
+        uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fi;
         for (int c0 = 0; c0 < it.n; c0 += 32) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(lane_base + c0, gv);
-          tmem_ld32(lane_base + 256 + c0, uv);
-          tmem_wait_ld();
-          if (ok) {
-            uint16_t* o = a.out + (long long)(it.r0 + c0) * a.out_ld + fi;
+          float v[32];
+          if (MODE == 0) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(lane_base + c0, gv);
+            tmem_ld32(lane_base + 256 + c0, uv);
+            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (c0 + j < it.n) {
-                const float g = __uint_as_float(gv[j]), u = __uint_as_float(uv[j]);
-                o[(long long)j * a.out_ld] = f32_to_bf16_bits(silu_f32(g) * u);
-              }
+              const float gg = __uint_as_float(gv[j]);
+              v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
             }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int fi = it.f0 + t * GM_ROWS + m;
-          const bool ok = fi < a.nrows;
-          for (int c0 = 0; c0 < it.n; c0 += 32) {
+          } else {
             uint32_t yv[32];
             tmem_ld32(lane_base + 256 * t + c0, yv);
             tmem_wait_ld();
-            if (ok) {
-              uint16_t* o = a.out + (long long)(it.r0 + c0) * a.out_ld + fi;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c0 + j < it.n) o[(long long)j * a.out_ld] = f32_to_bf16_bits(__uint_as_float(yv[j]));
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(yv[j]);
+          }
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const float send = odd ? v[2 * p] : v[2 * p + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float lo = odd ? recv : v[2 * p];
+            const float hi = odd ? v[2 * p + 1] : recv;
+            const int tok = c0 + 2 * p + odd;
+            if (ok && tok < it.n) {
+              const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+              *reinterpret_cast<uint32_t*>(obase + (long long)tok * a.out_ld) = w;
             }
           }
         }
@@ -499,14 +560,42 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_ffn_kernel(const GemmArgs 
 
 size_t ffn_gemm_ws_bytes(int, int, int, int, int) { return 0; }
 
+// ---------------------------------------------------------------- host side
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+void resolve_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+}
+
+// bf16 matrix [rows][cols] (row-major), box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_act_map(CUtensorMap* map, const void* ptr, long long rows, int cols, int box_rows) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 template <int QT, int MODE, class Tab>
-static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, cudaStream_t st) {
+static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, const CUtensorMap& map,
+                             cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   auto kern = gemm_ffn_kernel<QT, MODE, Tab>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
   if (err != cudaSuccess) return err;
-  kern<<<di->sm_count, GM_THREADS, GM_SMEM, st>>>(a, tab);
+  kern<<<di->sm_count, GM_THREADS, GM_SMEM, st>>>(a, tab, map);
   return cudaGetLastError();
 }
 
@@ -514,6 +603,10 @@ template <int QT, class Tab>
 static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
+  CUtensorMap xmap, hmap;
+  if (!make_act_map(&xmap, pb.x, pb.T, pb.H, 1) ||
+      !make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, GM_TOK))
+    return cudaErrorNotSupported;
   GemmArgs a{};
   a.offsets = pb.offsets;
   a.sorted_pair = pb.sorted_pair;
@@ -522,32 +615,33 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   a.status = di->status;
   a.act = pb.x;
   a.act_ld = pb.H;
+  a.K = pb.H;
   a.out = pb.h_act;
   a.out_ld = pb.I;
   a.wbase = pb.w13;
   a.wstride = (long long)pb.w13_bytes;
   a.table_off = 0;
   a.S = slabs_of(pb.H);
-  a.K = pb.H;
   a.nrows = pb.I;
   a.up_row0 = pb.I;
   a.ft_per_expert = (pb.I + GM_ROWS - 1) / GM_ROWS;
   GemmArgs d = a;
+  d.sorted_pair = nullptr;
   d.act = pb.h_act;
   d.act_ld = pb.I;
+  d.K = pb.I;
   d.out = pb.y_perm;
   d.out_ld = pb.H;
   d.wbase = pb.w2;
   d.wstride = (long long)tiles_bytes_per_expert(pb.qtype, pb.H, pb.I);
   d.table_off = (long long)pb.w13_bytes;
   d.S = slabs_of(pb.I);
-  d.K = pb.I;
   d.nrows = pb.H;
   d.up_row0 = 0;
   d.ft_per_expert = (pb.H + 2 * GM_ROWS - 1) / (2 * GM_ROWS);
-  cudaError_t err = gm_launch<QT, 0>(a, tab, st);
+  cudaError_t err = gm_launch<QT, 0>(a, tab, xmap, st);
   if (err != cudaSuccess) return err;
-  return gm_launch<QT, 1>(d, tab, st);
+  return gm_launch<QT, 1>(d, tab, hmap, st);
 }
 
 cudaError_t launch_ffn_gemm(const FfnProblem& pb, void*, size_t, cudaStream_t st) {

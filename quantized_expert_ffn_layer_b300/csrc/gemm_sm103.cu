@@ -3,26 +3,34 @@
 // its GGUF Q4_0 / MXFP4 banks, with the block decode of §六 fused into the operand
 // staging.
 //
-// One persistent CTA per SM.  A work item is (expert, 128 feature rows x 2 tiles,
-// up to 256 of the expert's token rows): for gate/up the two tiles are the gate and
-// the up rows of the same 128 features, for down two consecutive 128-row tiles of
-// the output.  Per 64-element reduction block ("stage"):
-//   * a loader warp copies the stage's 16 raw weight records (16 rows x 64 codes +
-//     scales each) into a ring of shared-memory slots with 1-D bulk copies, and the
-//     token rows into the 128-byte-swizzled K-major B tile with TMA tensor loads
-//     (one 64 x 256 box for the down projection, whose rows are contiguous; one
-//     64 x 1 box per row for gate/up, whose rows are gathered by the permutation);
-//   * 8 converter warps decode the raw records into exact bf16 (round-to-nearest-
-//     even of the decoded value) in the swizzled K-major A tiles;
+// One persistent CTA per SM.  A work item is (expert, a slice of weight rows, up to
+// 256 of the expert's token rows).  For gate/up the slice is 128 features: a tile of
+// their gate rows and a tile of their up rows, accumulated side by side in tensor
+// memory (columns [0, 256) and [256, 512)) so that the epilogue sees g and u of a
+// feature in one thread.  For down the slice is one 128-row tile, and two
+// accumulator buffers alternate so that the epilogue of one item overlaps the MMAs of
+// the next.  Per 64-element reduction block ("stage"):
+//   * a raw-weight warp copies the stage's weight records (16 rows x 64 codes +
+//     scales each) into a ring of shared-memory slots with 1-D bulk copies and warms
+//     L2 with the next item's records;
+//   * 8 converter warps decode the records into exact bf16 (round-to-nearest-even of
+//     the decoded value) in the 128-byte-swizzled K-major A tiles, and for gate/up
+//     also gather the item's token rows of x with cp.async into the B tile;
+//   * for down a token warp loads the (contiguous) rows of h with one TMA box;
 //   * one thread issues tcgen05.mma kind::f16 (M = 128 weight rows, N = the token
-//     count rounded up to 16, K = 16) into two fp32 accumulators in tensor memory
-//     (columns [0, 256) and [256, 512)) and commits each stage back to the ring;
-//   * 4 epilogue warps read the accumulators with tcgen05.ld and write
-//     h = silu(gate) * up (gate/up) or y (down) as bf16.
+//     count rounded up to 16, K = 16) and commits each stage back to the ring;
+//   * 4 epilogue warps read the accumulators with tcgen05.ld, compute
+//     h = silu(gate) * up or take y, and store bf16 rows through a small staging
+//     tile as 16-byte vectors.
 // The weights are the A operand (M) and the tokens the B operand (N), so a small
 // expert costs a narrow MMA rather than a mostly empty 128-row tile.  Items are
 // ordered expert by expert with the token tile innermost, so CTAs that run at the
 // same time share weight tiles through L2.
+//
+// A-tile row order: weight row r of a 16-row record is stored at tile row
+// sigma(r) (rows 0..3 -> 0,2,4,6, rows 4..7 -> 1,3,5,7, and the same +8 for rows
+// 8..15).  With it the converter stores of a quarter-warp fall on 8 different
+// 16-byte bank groups of the swizzled rows; the epilogue maps TMEM lanes back.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,32 +45,49 @@ namespace ftmoe {
 
 constexpr int GM_TOK = 256;         // token rows per item (largest MMA N)
 constexpr int GM_ROWS = 128;        // weight rows per tile (MMA M)
-constexpr int GM_NS = 3;            // A/B operand stages
-constexpr int GM_NR = 3;            // raw weight stages
 constexpr int GM_EPI_WARPS = 4;     // warps 0..3 (one per TMEM lane quarter)
 constexpr int GM_MMA_WARP = 4;      // TMEM owner; lane 0 issues the MMAs
 constexpr int GM_RAW_WARP = 5;      // bulk copies of the raw weight records
-constexpr int GM_TOK_WARP = 6;      // token rows: TMA box (down) or cp.async gather (gate/up)
-constexpr int GM_CONV0 = 7;         // first converter warp
-constexpr int GM_CONV_WARPS = 8;
-constexpr int GM_THREADS = (GM_CONV0 + GM_CONV_WARPS) * 32;  // 480
+constexpr int GM_TOK_WARP = 6;      // token rows of the down projection (TMA); warp 7 idles
+constexpr int GM_CONV0 = 8;         // first converter warp
+constexpr int GM_CONV_WARPS = 16;
+constexpr int GM_CONV_THREADS = GM_CONV_WARPS * 32;
+constexpr int GM_THREADS = (GM_CONV0 + GM_CONV_WARPS) * 32;  // 768
 constexpr uint32_t GM_TMEM_COLS = 512;
-constexpr int GM_A_TILE = GM_ROWS * 128;           // 16 KB of bf16 (128 rows x 64)
-constexpr int GM_B_TILE = GM_TOK * 128;            // 32 KB of bf16 (256 rows x 64)
-constexpr int GM_STAGE = 2 * GM_A_TILE + GM_B_TILE;
-constexpr int GM_RAW_STAGE = 16 * 576;             // 16 records (Q4_0 size; MXFP4 uses less)
+constexpr int GM_A_TILE = GM_ROWS * 128;  // 16 KB of bf16 (128 rows x 64)
+constexpr int GM_B_TILE = GM_TOK * 128;   // 32 KB of bf16 (256 rows x 64)
+constexpr int GM_ECOL = 16;               // accumulator columns (tokens) per epilogue step
+constexpr int GM_STG = GM_ECOL * 64;      // epilogue staging per warp: 16 rows x 32 bf16
 constexpr int GM_MAX_E = 1024;
 
+// Per-projection layout: gate/up stages hold two A tiles, down stages one.
+template <int MODE>
+struct GmCfg {
+  static constexpr int NT = MODE == 0 ? 2 : 1;           // A tiles (MMAs per k-step)
+  static constexpr int NACC = MODE == 0 ? 1 : 2;         // accumulator buffers
+  static constexpr int NS = MODE == 0 ? 3 : 4;           // operand stages
+  static constexpr int NR = MODE == 0 ? 2 : 4;           // raw weight stages
+  static constexpr int NREC = 8 * NT;                    // records per stage
+  static constexpr int STAGE = NT * GM_A_TILE + GM_B_TILE;
+  static constexpr int RAW_STAGE = NREC * 576;
+  static constexpr int TPR = GM_CONV_THREADS / NREC;     // converter threads per record
+  static constexpr int NSTEP = 4 * 16 / TPR;              // 16-element steps per thread
+};
+
 struct GemmTail {
-  uint64_t a_full[GM_NS], b_full[GM_NS], empty[GM_NS];
-  uint64_t raw_full[GM_NR], raw_empty[GM_NR];
-  uint64_t acc_full, acc_empty, drain;
+  uint64_t a_full[4], b_full[4], empty[4];
+  uint64_t raw_full[4], raw_empty[4];
+  uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
   int citem[GM_MAX_E + 1];  // exclusive prefix of items per expert
 };
-constexpr size_t GM_SMEM =
-    1024 + (size_t)GM_NS * GM_STAGE + (size_t)GM_NR * GM_RAW_STAGE + sizeof(GemmTail);
+template <int MODE>
+constexpr size_t gm_smem_bytes() {
+  return 1024 + (size_t)GmCfg<MODE>::NS * GmCfg<MODE>::STAGE +
+         (size_t)GmCfg<MODE>::NR * GmCfg<MODE>::RAW_STAGE + (size_t)GM_EPI_WARPS * GM_STG +
+         sizeof(GemmTail);
+}
 
 struct GemmArgs {
   const int32_t* offsets;
@@ -79,7 +104,7 @@ struct GemmArgs {
   int K;                 // reduction length
   int nrows;             // output rows of the projection's result: I or H
   int up_row0;           // gate/up: first up row of w13 (= I)
-  int ft_per_expert;     // feature items per token tile
+  int ft_per_expert;     // weight-row slices per token tile
   int* status;
 };
 
@@ -114,7 +139,7 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   const int ft = local / ntt, tt = local - ft * ntt;
   it.r0 = beg + tt * GM_TOK;
   it.n = min(GM_TOK, ne - tt * GM_TOK);
-  it.f0 = MODE == 0 ? ft * GM_ROWS : ft * 2 * GM_ROWS;
+  it.f0 = ft * GM_ROWS;
   return it;
 }
 
@@ -123,15 +148,17 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
 template <int MODE>
 __device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const GemmArgs& a,
                                              bool& ok) {
-  const int t = ri >> 3, rg = ri & 7;
-  if (MODE == 0) {
-    const int row = it.f0 + rg * 16;
-    ok = row < a.nrows;
-    return t ? row + a.up_row0 : row;
-  }
-  const int row = it.f0 + t * GM_ROWS + rg * 16;
+  const int row = it.f0 + (ri & 7) * 16;
   ok = row < a.nrows;
-  return row;
+  return (MODE == 0 && (ri >> 3)) ? row + a.up_row0 : row;
+}
+
+__host__ __device__ constexpr int gm_sigma(int r) {
+  return (r & 8) | ((r & 7) < 4 ? 2 * (r & 3) : 2 * (r & 3) + 1);
+}
+__device__ __forceinline__ int gm_sigma_inv(int t) {
+  const int u = t & 7;
+  return (t & 8) | ((u & 1) ? 4 + (u >> 1) : (u >> 1));
 }
 
 // ---------------------------------------------------------------- weight decode
@@ -165,18 +192,29 @@ __device__ __forceinline__ uint4 decode8(uint32_t W, uint32_t s_hi, uint32_t s_l
   return make_uint4(r[0], r[2], r[1], r[3]);
 }
 
-// fp16 scale -> (hi, lo) bf16x2 pairs with hi + lo == d exactly.
-__device__ __forceinline__ void split_scale(uint32_t h16, uint32_t& hi2, uint32_t& lo2) {
-  const float d = half_bits_to_f32(h16);
-  const uint32_t hi = f32_to_bf16_bits(d);
-  const uint32_t lo = f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
-  hi2 = hi | (hi << 16);
-  lo2 = lo | (lo << 16);
+// Block scale of one row as (hi, lo) bf16x2 pairs with hi + lo == the scale exactly
+// (Q4_0 fp16 d), or (2^(e-127), 0) for an MXFP4 E8M0 byte.
+template <int QT>
+__device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
+  if (QT == FTMOE_Q4_0) {
+    const float d = half_bits_to_f32(bits);
+    const uint32_t hi = f32_to_bf16_bits(d);
+    const uint32_t lo = f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
+    hi2 = hi | (hi << 16);
+    lo2 = lo | (lo << 16);
+  } else {
+    const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
+    hi2 = b | (b << 16);
+    lo2 = 0;
+  }
 }
 
-__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
-  const uint32_t b = e == 0 ? 0x0040u : (e == 255 ? 0x7FC0u : (e << 7));
-  return b | (b << 16);
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
@@ -194,69 +232,88 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 
-// Permutes the four words so that w[s] becomes the old w[s ^ h] (h = 0..3).
-__device__ __forceinline__ void xperm4(uint32_t (&w)[4], int h) {
-  if (h & 1) {
-    uint32_t t = w[0]; w[0] = w[1]; w[1] = t;
-    t = w[2]; w[2] = w[3]; w[3] = t;
-  }
-  if (h & 2) {
-    uint32_t t = w[0]; w[0] = w[2]; w[2] = t;
-    t = w[1]; w[1] = w[3]; w[3] = t;
-  }
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
-// One converter thread's share of a record: the 32 code bytes of record lanes 4g + 2m
-// and 4g + 2m + 1 (elements 8m..8m+7 of each 16-element step of rows g and g + 8),
-// decoded into rows rg*16 + g and rg*16 + g + 8 of the A tile.
-template <int QT>
-__device__ __forceinline__ void convert_record(uint32_t rec, uint32_t tile, int rg, int g, int m) {
-  const uint4 ca = lds128(rec + (4 * g + 2 * m) * 16);
-  const uint4 cb = lds128(rec + (4 * g + 2 * m + 1) * 16);
-  uint32_t shi[2][2], slo[2][2];  // [block][row half]
-  if (QT == FTMOE_Q4_0) {
-    uint32_t s0, s1;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(s0), "=r"(s1)
-                 : "r"(rec + REC_CODE_BYTES + g * 8)
-                 : "memory");
-    split_scale(s0 & 0xFFFFu, shi[0][0], slo[0][0]);
-    split_scale(s0 >> 16, shi[0][1], slo[0][1]);
-    split_scale(s1 & 0xFFFFu, shi[1][0], slo[1][0]);
-    split_scale(s1 >> 16, shi[1][1], slo[1][1]);
-  } else {
-    uint32_t s0;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s0) : "r"(rec + REC_CODE_BYTES + g * 4) : "memory");
+// Four bf16x2 (128 + q) pairs from nibble bytes: E1 holds elements 0..3 and E2 elements
+// 4..7 of one row as byte-aligned nibbles in the order (e0, e2, e1, e3).
+__device__ __forceinline__ void q4_pairs(uint32_t E1, uint32_t E2, uint32_t (&t)[4]) {
+  const uint32_t K = 0x43434343u;  // high byte of bf16 128
+  t[0] = prmt(E1, K, 0x4240u);
+  t[1] = prmt(E1, K, 0x4341u);
+  t[2] = prmt(E2, K, 0x4240u);
+  t[3] = prmt(E2, K, 0x4341u);
+}
+
+// (128 + q) pairs -> RNE((q - 8) * d) with d = hi + lo split exactly (see row_scale).
+__device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi, uint32_t s_lo) {
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+  uint32_t r[4];
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        shi[b][h] = e8m0_bf16x2((s0 >> (8 * (2 * b + h))) & 0xFFu);
-        slo[b][h] = 0;
-      }
+  for (int p = 0; p < 4; ++p) {
+    const __nv_bfloat162 u = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t[p]), off);
+    const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
+    const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
+    r[p] = *reinterpret_cast<const uint32_t*>(&w);
   }
-  uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-  uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-  // step s handles word j = s ^ h(g): with the row swizzle (chunk ^ g) this puts the
-  // 8 lanes of each quarter-warp on 8 different 16-byte bank groups
-  const int hx = (((g >> 1) & 1) << 1) | ((g ^ (g >> 1)) & 1);
-  xperm4(wa, hx);
-  xperm4(wb, hx);
-  const uint32_t row0 = tile + (2 * rg) * 1024 + g * 128;  // row rg*16 + g
-  const uint32_t row1 = row0 + 1024;                       // row rg*16 + g + 8
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// One converter thread's share of a record in shared memory.  Record lanes 4g + 2m (A)
+// and 4g + 2m + 1 (B) hold elements 8m..8m+7 of each 16-element step j of rows g and
+// g + 8 (A: elements 8m..8m+3, B: 8m+4..8m+7).  The thread decodes NSTEP steps starting
+// at J0 (NSTEP = 2: quantization block J0 / 2; NSTEP = 1: one step) of both rows into the
+// A tile.  Lane pairs (m = 0, 1) share the scale conversions through one shuffle.  The
+// two 16-byte code loads are issued in an order that depends on (g >> 1) & 1 so that
+// each quarter-warp reads 8 different bank groups.
+template <int QT, int NSTEP, int J0>
+__device__ __forceinline__ void convert_record(uint32_t rec, uint32_t tile, int rg, int g, int m) {
+  constexpr int BLK = J0 >> 1;  // quantization block of the thread's steps
+  const int sw = (g >> 1) & 1;
+  const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
+  const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
+  const uint4 ca = sw ? l2 : l1, cb = sw ? l1 : l2;
+  const int T0 = rg * 16 + gm_sigma(g);  // tile row of record row g (row g + 8: T0 + 8)
+  const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
+  const uint32_t row1 = row0 + 1024;
+  const uint32_t ph = (uint32_t)(T0 & 7);
+  // scale of row g + 8 m (this lane) and of the other row (partner lane)
+  uint32_t sbits;
+  {
+    const int idx = (g * 2 + BLK) * 2 + m;
+    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
+    uint32_t w;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(rec + REC_CODE_BYTES + (byte & ~3)) : "memory");
+    sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
+  }
+  uint32_t mh, ml;
+  row_scale<QT>(sbits, mh, ml);
+  const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
+  const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
+  const uint32_t sh0 = m ? oh : mh, sl0 = m ? ol : ml;
+  const uint32_t sh1 = m ? mh : oh, sl1 = m ? ml : ol;
+  const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+  const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int j = s ^ hx;
-    const int b = j >> 1;
-    const uint32_t A = wa[s], B = wb[s];
-    const uint32_t wg = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
-    const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
-    const uint32_t sh0 = b ? shi[1][0] : shi[0][0], sl0 = b ? slo[1][0] : slo[0][0];
-    const uint32_t sh1 = b ? shi[1][1] : shi[0][1], sl1 = b ? slo[1][1] : slo[0][1];
-    const uint32_t cp = 2 * j + m;
-    const uint32_t off = ((cp ^ (uint32_t)g) * 16);
-    sts128(row0 + off, decode8<QT>(wg, sh0, sl0));
-    sts128(row1 + off, decode8<QT>(wg8, sh1, sl1));
+  for (int s = 0; s < NSTEP; ++s) {
+    const int j = J0 + s;
+    const uint32_t A = wa[j], Bw = wb[j];
+    const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
+    if (QT == FTMOE_Q4_0) {
+      uint32_t t0[4], t1[4];
+      q4_pairs(A & 0x0F0F0F0Fu, Bw & 0x0F0F0F0Fu, t0);                // row g
+      q4_pairs((A >> 4) & 0x0F0F0F0Fu, (Bw >> 4) & 0x0F0F0F0Fu, t1);  // row g + 8
+      sts128(row0 + off, q4_scale(t0, sh0, sl0));
+      sts128(row1 + off, q4_scale(t1, sh1, sl1));
+    } else {
+      const uint32_t wg = (A & 0x0F0F0F0Fu) | ((Bw & 0x0F0F0F0Fu) << 4);
+      const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (Bw & 0xF0F0F0F0u);
+      sts128(row0 + off, decode8<QT>(wg, sh0, sl0));
+      sts128(row1 + off, decode8<QT>(wg8, sh1, sl1));
+    }
   }
 }
 
@@ -291,29 +348,33 @@ template <int QT, int MODE, class Tab>
 __global__ void __launch_bounds__(GM_THREADS, 1)
     gemm_ffn_kernel(const GemmArgs a, const __grid_constant__ Tab tab,
                     const __grid_constant__ CUtensorMap act_map) {
+  using C = GmCfg<MODE>;
   constexpr int RB = rec_bytes(QT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_addr - raw_addr);
-  const uint32_t rawring = base_addr + GM_NS * GM_STAGE;
-  GemmTail& tl =
-      *reinterpret_cast<GemmTail*>(base + (size_t)GM_NS * GM_STAGE + (size_t)GM_NR * GM_RAW_STAGE);
+  const uint32_t rawring = base_addr + C::NS * C::STAGE;
+  const uint32_t staging = rawring + C::NR * C::RAW_STAGE;
+  GemmTail& tl = *reinterpret_cast<GemmTail*>(base + (size_t)C::NS * C::STAGE +
+                                              (size_t)C::NR * C::RAW_STAGE + GM_EPI_WARPS * GM_STG);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &tl.abort_flag;
 
   if (tid == 0) {
-    for (int s = 0; s < GM_NS; ++s) {
+    for (int s = 0; s < C::NS; ++s) {
       mbar_init(&tl.a_full[s], GM_CONV_WARPS);
       mbar_init(&tl.b_full[s], 1);
       mbar_init(&tl.empty[s], 1);
     }
-    for (int s = 0; s < GM_NR; ++s) {
+    for (int s = 0; s < C::NR; ++s) {
       mbar_init(&tl.raw_full[s], 1);
       mbar_init(&tl.raw_empty[s], GM_CONV_WARPS);
     }
-    mbar_init(&tl.acc_full, 1);
-    mbar_init(&tl.acc_empty, GM_EPI_WARPS * 32);
+    for (int b = 0; b < C::NACC; ++b) {
+      mbar_init(&tl.acc_full[b], 1);
+      mbar_init(&tl.acc_empty[b], GM_EPI_WARPS * 32);
+    }
     mbar_init(&tl.drain, 1);
     tl.abort_flag = 0;
     fence_barrier_init();
@@ -322,7 +383,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     tmem_alloc(&tl.tmem_base, GM_TMEM_COLS);
     tmem_relinquish();
   }
-  // items per expert: ceil(n_e / 256) token tiles x feature items
+  // items per expert: ceil(n_e / 256) token tiles x weight-row slices
   if (warp == 0) {
     int carry = 0;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
@@ -353,14 +414,14 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     uint32_t rphase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
-      // lane r < 16: record r of every stage (tile r / 8, row group r % 8)
+      // lane r < NREC: record r of every stage (tile r / 8, row group r % 8)
       bool rok = false;
       const uint8_t* rec0 = nullptr;
-      if (lane < 16)
+      if (lane < C::NREC)
         rec0 = tab.get(it.e, a) + (long long)(gm_record_row<MODE>(it, lane, a, rok) / 16) * a.S * RB;
-      const int nrec = __popc(__ballot_sync(0xffffffffu, lane < 16 && rok));
+      const int nrec = __popc(__ballot_sync(0xffffffffu, lane < C::NREC && rok));
       // warm L2 with the CTA's next item's records while this one streams
-      if (i + G < nitems && lane < 16) {
+      if (i + G < nitems && lane < C::NREC) {
         const GmItem nx = gm_item<MODE>(i + G, a, tl.citem);
         bool nok;
         const int nrow = gm_record_row<MODE>(nx, lane, a, nok);
@@ -370,10 +431,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         if (!mbar_wait_or_abort(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
         if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * RB));
         __syncwarp();
-        if (lane < 16 && rok)
-          bulk_g2s(base + GM_NS * GM_STAGE + rslot * GM_RAW_STAGE + lane * RB,
+        if (lane < C::NREC && rok)
+          bulk_g2s(base + C::NS * C::STAGE + rslot * C::RAW_STAGE + lane * RB,
                    rec0 + (long long)kb * RB, RB, &tl.raw_full[rslot]);
-        if (++rslot == GM_NR) { rslot = 0; rphase ^= 1u; }
+        if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
       }
       if (*abort_flag) break;
     }
@@ -389,10 +450,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&tl.b_full[slot], (uint32_t)GM_B_TILE);
-            tma_load_2d(base_addr + slot * GM_STAGE + 2 * GM_A_TILE, &act_map, kb * 64, it.r0,
+            tma_load_2d(base_addr + slot * C::STAGE + C::NT * GM_A_TILE, &act_map, kb * 64, it.r0,
                         &tl.b_full[slot]);
           }
-          if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
+          if (++slot == C::NS) { slot = 0; phase ^= 1u; }
         }
         if (*abort_flag) break;
       }
@@ -400,72 +461,111 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   } else if (warp >= GM_CONV0) {
     // ------------------------------------------------------------ converters
     const int ct = tid - GM_CONV0 * 32;
-    const int ri = (ct >> 5) * 2 + (lane >> 4);  // record of the stage
+    const int cw = ct >> 5;  // converter warp
+    // each warp converts the same steps of two records (lanes 0..15 and 16..31):
+    // gate/up: records 2 (cw / 2) + {0, 1}, quantization block cw % 2;
+    // down:    records 2 (cw % 4) + {0, 1}, 16-element step cw / 4
+    const int ri = (MODE == 0 ? 2 * (cw >> 1) : 2 * (cw & 3)) + (lane >> 4);
+    const int jsel = MODE == 0 ? (cw & 1) : (cw >> 2);
     const int g = (lane & 15) >> 1, m = lane & 1;
     int slot = 0, rslot = 0;
     uint32_t phase = 0, rphase = 0;
-    // gate/up token rows: this thread copies 16-byte chunk (ct & 7) of rows (ct >> 3) + 32 r
+    // gate/up token rows: this thread copies 16-byte chunk (ct & 7) of rows (ct >> 3) + 64 r,
+    // one stage ahead of the conversion so that the copies land while it decodes
+    constexpr int RPT = GM_TOK * 8 / GM_CONV_THREADS;  // rows per thread
     const int ch = ct & 7;
+    int bi = blockIdx.x, bkb = 0, bslot = 0;
+    uint32_t bphase = 0;
+    const uint16_t* rowp[RPT];
+    auto load_rows = [&](int item) {
+      const GmItem it = gm_item<MODE>(item, a, tl.citem);
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const int rr = (ct >> 3) + (GM_CONV_THREADS / 8) * r;
+        rowp[r] = nullptr;
+        if (rr < it.n) {
+          const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + rr] / a.k : (it.r0 + rr);
+          rowp[r] = a.act + ar * a.act_ld + ch * 8;
+        }
+      }
+    };
+    auto issue_rows = [&]() -> bool {  // copies of stage (bi, bkb); false when none / aborted
+      if (bi >= nitems) return false;
+      if (!mbar_wait_or_abort(&tl.empty[bslot], bphase ^ 1u, abort_flag, a.status)) return false;
+      const uint32_t bt = base_addr + bslot * C::STAGE + C::NT * GM_A_TILE;
+      const bool kok = bkb * 64 + ch * 8 < a.K;  // beyond K: zeros
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        if (rowp[r]) {
+          const int rr = (ct >> 3) + (GM_CONV_THREADS / 8) * r;
+          cp_async16(bt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16),
+                     kok ? rowp[r] + bkb * 64 : rowp[r], kok ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (++bslot == C::NS) { bslot = 0; bphase ^= 1u; }
+      if (++bkb == a.S) {
+        bkb = 0;
+        bi += G;
+        if (bi < nitems) load_rows(bi);
+      }
+      return true;
+    };
+    if (MODE == 0 && bi < nitems) {
+      load_rows(bi);
+      issue_rows();
+    }
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       bool rok;
       gm_record_row<MODE>(it, ri, a, rok);
-      const uint16_t* rowp[8];
-      if (MODE == 0) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int rr = (ct >> 3) + 32 * r;
-          rowp[r] = nullptr;
-          if (rr < it.n) {
-            const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + rr] / a.k : (it.r0 + rr);
-            rowp[r] = a.act + ar * a.act_ld + ch * 8;
-          }
-        }
-      }
       for (int kb = 0; kb < a.S; ++kb) {
+        const bool ahead = MODE == 0 && issue_rows();
         if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
         if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
-        const uint32_t st_addr = base_addr + slot * GM_STAGE;
-        if (MODE == 0) {
-          const uint32_t bt = st_addr + 2 * GM_A_TILE;
-          const bool kok = kb * 64 + ch * 8 < a.K;  // beyond K: zeros
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            if (rowp[r]) {
-              const int rr = (ct >> 3) + 32 * r;
-              cp_async16(bt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16),
-                         kok ? rowp[r] + kb * 64 : rowp[r], kok ? 16u : 0u);
+        if (rok) {
+          const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
+          const uint32_t tile = base_addr + slot * C::STAGE + (ri >> 3) * GM_A_TILE;
+          if (MODE == 0) {
+            if (jsel) convert_record<QT, 2, 2>(rec, tile, ri & 7, g, m);
+            else convert_record<QT, 2, 0>(rec, tile, ri & 7, g, m);
+          } else {
+            switch (jsel) {
+              case 0: convert_record<QT, 1, 0>(rec, tile, ri & 7, g, m); break;
+              case 1: convert_record<QT, 1, 1>(rec, tile, ri & 7, g, m); break;
+              case 2: convert_record<QT, 1, 2>(rec, tile, ri & 7, g, m); break;
+              default: convert_record<QT, 1, 3>(rec, tile, ri & 7, g, m); break;
             }
           }
-          cp_async_commit();
         }
-        if (rok)
-          convert_record<QT>(rawring + rslot * GM_RAW_STAGE + ri * RB, st_addr + (ri >> 3) * GM_A_TILE,
-                             ri & 7, g, m);
-        if (MODE == 0) cp_async_wait<0>();
+        if (MODE == 0) {
+          if (ahead) cp_async_wait<1>(); else cp_async_wait<0>();  // this stage's rows have landed
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&tl.raw_empty[rslot]);
           mbar_arrive(&tl.a_full[slot]);
         }
-        if (++rslot == GM_NR) { rslot = 0; rphase ^= 1u; }
-        if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
+        if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+        if (++slot == C::NS) { slot = 0; phase ^= 1u; }
       }
       if (*abort_flag) break;
     }
+    if (MODE == 0) cp_async_wait<0>();
   } else if (warp == GM_MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      int slot = 0;
+      int slot = 0, buf = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < nitems && ok; i += G) {
         const GmItem it = gm_item<MODE>(i, a, tl.citem);
         const int N = max(16, (it.n + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(GM_ROWS, N);
-        if (!mbar_wait_or_abort(&tl.acc_empty, acc_phase ^ 1u, abort_flag, a.status)) break;
+        if (!mbar_wait_or_abort(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
+        const uint32_t d0 = tmem + buf * 256;
         for (int kb = 0; kb < a.S; ++kb) {
           if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status) ||
               (MODE == 1 && !mbar_wait_or_abort(&tl.b_full[slot], phase, abort_flag, a.status))) {
@@ -473,80 +573,89 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sa = base_addr + slot * GM_STAGE;
+          const uint32_t sa = base_addr + slot * C::STAGE;
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t bd = sdesc_kmajor_sw128(sa + 2 * GM_A_TILE + 32 * k16);
+            const uint64_t bd = sdesc_kmajor_sw128(sa + C::NT * GM_A_TILE + 32 * k16);
             const uint32_t acc = (kb | k16) ? 1u : 0u;
-            mma_bf16(tmem, sdesc_kmajor_sw128(sa + 32 * k16), bd, idesc, acc);
-            mma_bf16(tmem + 256, sdesc_kmajor_sw128(sa + GM_A_TILE + 32 * k16), bd, idesc, acc);
+            mma_bf16(d0, sdesc_kmajor_sw128(sa + 32 * k16), bd, idesc, acc);
+            if (C::NT == 2)
+              mma_bf16(d0 + 256, sdesc_kmajor_sw128(sa + GM_A_TILE + 32 * k16), bd, idesc, acc);
           }
           mma_commit(&tl.empty[slot]);
-          if (++slot == GM_NS) { slot = 0; phase ^= 1u; }
+          if (++slot == C::NS) { slot = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&tl.acc_full);
-        acc_phase ^= 1u;
+        mma_commit(&tl.acc_full[buf]);
+        if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
       }
       // every MMA issued above has finished once this arrives
       mma_commit(&tl.drain);
       mbar_wait_or_abort(&tl.drain, 0, abort_flag, a.status, 100000000ull);
     }
     __syncwarp();
-  } else {
+  } else if (warp < GM_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue (warps 0..3)
     const int q = warp;  // TMEM lanes [32q, 32q + 32)
+    // TMEM lane 32q + lane holds feature 32q + fl of the item (tile row order -> features)
+    const int fl = (lane & 16) + gm_sigma_inv(lane & 15);
+    // lanes l and l ^ 2 hold adjacent features fl and fl ^ 1
+    const int odd = fl & 1;
+    const uint32_t stg = staging + q * GM_STG;
+    int buf = 0;
     uint32_t acc_phase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
-      if (!mbar_wait_or_abort(&tl.acc_full, acc_phase, abort_flag, a.status)) break;
-      acc_phase ^= 1u;
+      if (!mbar_wait_or_abort(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
-      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-      // Lanes 2p and 2p + 1 swap values so that each stores two adjacent features (one
-      // bf16x2 word): the even lane for the even tokens, the odd lane for the odd ones.
-      const int odd = lane & 1;
-      const int fpair = 32 * q + (lane & ~1);  // first feature of the pair within the item
-#pragma unroll 1
-      for (int t = 0; t < (MODE == 0 ? 1 : 2); ++t) {
-        const int fi = it.f0 + t * GM_ROWS + fpair;
-        const bool ok = fi < a.nrows;
-        uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fi;
-        for (int c0 = 0; c0 < it.n; c0 += 32) {
-          float v[32];
-          if (MODE == 0) {
-            uint32_t gv[32], uv[32];
-            tmem_ld32(lane_base + c0, gv);
-            tmem_ld32(lane_base + 256 + c0, uv);
-            tmem_wait_ld();
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
+      // Each 32 x 16 block (this warp's 32 features x 16 tokens) goes through the warp's
+      // staging tile [token][feature] so that the global stores are 16-byte vectors.
+      const int fw = it.f0 + 32 * q;  // first feature of this warp
+      const bool ok = fw < a.nrows;
+      uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
+      for (int c0 = 0; c0 < it.n; c0 += GM_ECOL) {
+        float v[GM_ECOL];
+        if (MODE == 0) {
+          uint32_t gv[GM_ECOL], uv[GM_ECOL];
+          tmem_ld16(lane_base + c0, gv);
+          tmem_ld16(lane_base + 256 + c0, uv);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float gg = __uint_as_float(gv[j]);
-              v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
-            }
-          } else {
-            uint32_t yv[32];
-            tmem_ld32(lane_base + 256 * t + c0, yv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(yv[j]);
+          for (int j = 0; j < GM_ECOL; ++j) {
+            const float gg = __uint_as_float(gv[j]);
+            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
           }
+        } else {
+          uint32_t yv[GM_ECOL];
+          tmem_ld16(lane_base + c0, yv);
+          tmem_wait_ld();
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const float send = odd ? v[2 * p] : v[2 * p + 1];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const float lo = odd ? recv : v[2 * p];
-            const float hi = odd ? v[2 * p + 1] : recv;
-            const int tok = c0 + 2 * p + odd;
-            if (ok && tok < it.n) {
-              const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
-              *reinterpret_cast<uint32_t*>(obase + (long long)tok * a.out_ld) = w;
-            }
-          }
+          for (int j = 0; j < GM_ECOL; ++j) v[j] = __uint_as_float(yv[j]);
         }
+#pragma unroll
+        for (int p = 0; p < GM_ECOL / 2; ++p) {
+          const float send = odd ? v[2 * p] : v[2 * p + 1];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
+          const float lo = odd ? recv : v[2 * p];
+          const float hi = odd ? v[2 * p + 1] : recv;
+          const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (fl & ~1) * 2), "r"(w)
+                       : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r4 = 0; r4 < GM_ECOL / 8; ++r4) {
+          const int row = 8 * r4 + (lane >> 2);
+          const uint4 d = lds128(stg + row * 64 + (lane & 3) * 16);
+          if (ok && c0 + row < it.n)
+            *reinterpret_cast<uint4*>(obase + (long long)(c0 + row) * a.out_ld) = d;
+        }
+        __syncwarp();
       }
       tc_fence_before_sync();
-      mbar_arrive(&tl.acc_empty);
+      mbar_arrive(&tl.acc_empty[buf]);
+      if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -593,9 +702,11 @@ static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   auto kern = gemm_ffn_kernel<QT, MODE, Tab>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+  constexpr size_t smem = gm_smem_bytes<MODE>();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<di->sm_count, GM_THREADS, GM_SMEM, st>>>(a, tab, map);
+  kern<<<di->sm_count, GM_THREADS, smem, st>>>(a, tab, map);
   return cudaGetLastError();
 }
 
@@ -638,7 +749,7 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   d.S = slabs_of(pb.I);
   d.nrows = pb.H;
   d.up_row0 = 0;
-  d.ft_per_expert = (pb.H + 2 * GM_ROWS - 1) / (2 * GM_ROWS);
+  d.ft_per_expert = (pb.H + GM_ROWS - 1) / GM_ROWS;
   cudaError_t err = gm_launch<QT, 0>(a, tab, xmap, st);
   if (err != cudaSuccess) return err;
   return gm_launch<QT, 1>(d, tab, hmap, st);

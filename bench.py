@@ -90,6 +90,7 @@ class ClockSampler:
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "expert_ffn_gemv": ["gemv.cu", "common.cuh", "pipeline.cuh"],
+    "expert_ffn_gemm": ["gemm_sm103.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
 }
 
 
@@ -166,7 +167,7 @@ def run_reference(args, cfg, L, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=["decode", "prefill", "tiny"])
@@ -175,6 +176,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the extra prefill-layer measurement of the default run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -207,146 +210,48 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    from quantized_expert_ffn_layer_b300 import MoELayer
-    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    from quantized_expert_ffn_layer_b300 import ftmoe as F  # noqa: F401  (fails loudly without libftmoe)
 
-    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev)
-    T, k = L.T, L.k
-    x = torch.from_numpy(L.x.view(np.int16)).to(dev).view(torch.bfloat16)
-    lg = torch.from_numpy(L.logits).to(dev)
-    out = torch.empty((T, L.H), dtype=torch.bfloat16, device=dev)
-    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
-    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        m.forward(lg, x, k, out=out, ids_out=ids, w_out=wts)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    U = unique_experts(ids.cpu().numpy())
-
-    # ---- timed region: K steps, L2 flushed between steps (outside the events)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    my_ms = float(np.sum(step_ms))
-    max_ms = my_ms
-    if pg:
-        t = torch.tensor([my_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        max_ms = float(t.item())
-    tokens_all = T * args.steps * world
-    value = tokens_all / (max_ms / 1e3)
-
-    # ---- dominant kernel: the expert FFN step (gate/up+SwiGLU GEMV, down GEMV),
-    # timed alone on the same stream with its inputs from the route/permute above
-    E, H, I = L.E, L.H, L.I
-    P = T * k
-    ws_ffn_n = F.ftmoe_ffn_workspace_bytes(T, k, E, H, I)
-    ws_ffn = torch.empty(max(ws_ffn_n, 256), dtype=torch.uint8, device=dev)
-    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    sp = torch.empty(P, dtype=torch.int32, device=dev)
-    inv = torch.empty(P, dtype=torch.int32, device=dev)
-    pws_n = F.ftmoe_permute_workspace_bytes(T, k, E)
-    pws = torch.empty(max(pws_n, 256), dtype=torch.uint8, device=dev)
-    F.ftmoe_permute(ids, T, k, E, offs, sp, inv, pws, pws_n)
-    y_perm = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
-    for _ in range(3):
-        F.ftmoe_expert_ffn(m.weights, x, T, k, offs, sp, y_perm, ws_ffn, ws_ffn_n)
-    kt = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        F.ftmoe_expert_ffn(m.weights, x, T, k, offs, sp, y_perm, ws_ffn, ws_ffn_n)
-        b.record(stream)
-        kt.append((a, b))
-    torch.cuda.synchronize()
-    ffn_ms = float(np.mean([a.elapsed_time(b) for a, b in kt]))
-    blob = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
-    alg_bytes = U * blob + P * H * 2 + P * H * 2 + T * H * 2 + P * I * 2 * 2
     pk, pk_kind = peaks()
-    hbm = float(pk["hbm_gbs"])
-    achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "expert FFN (gate/up+SwiGLU GEMV, down GEMV)",
-                "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_kind": f"{pk_kind} hbm_gbs (copy)",
-                "traffic": recorded_traffic("expert_ffn_gemv", cfg["workload"]),
-                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": ffn_ms, "unique_experts": U}
-    layer_bytes = alg_bytes + T * E * 4
-    layer_frac = layer_bytes / (np.mean(step_ms) / 1e3) / 1e9 / hbm
 
-    # ---- end to end through the C ABI with host buffers
-    x_h = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    lg_h = torch.from_numpy(L.logits).pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    lg_d = torch.empty_like(lg)
-
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        m.forward(lg_d, x_d, k, out=out)
-        out_h.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    ee = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        ee.append((a, b))
-    torch.cuda.synchronize()
-    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in ee]))
-    e2e_ms_max = e2e_ms
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms_max = float(t.item())
-    e2e_val = tokens_all / (e2e_ms_max / 1e3)
+    clk = ClockSampler(local_rank)
+    head = measure_layer(L, dev, args.steps, args.warmup, flush, stream, pg, clk=clk)
+    U = head["U"]
+    T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
+    P = T * k
+    tokens_all = T * args.steps * world
+    value = tokens_all / (head["max_ms"] / 1e3)
+    roofline = ffn_roofline(L, U, head["ffn_ms"], pk, pk_kind, cfg["workload"])
+    e2e_val = tokens_all / (head["e2e_max_ms"] / 1e3)
 
     # ---- decode sweep over the other batch sizes (informative)
     sweep = {}
     if not args.no_sweep and args.config == "decode":
         for Ts in CONFIGS["decode"]["T_sweep"]:
             if Ts == T:
-                sweep[str(Ts)] = {"tokens_per_s": value, "ms": float(np.mean(step_ms))}
+                sweep[str(Ts)] = {"tokens_per_s": value, "ms": float(np.mean(head["step_ms"]))}
                 continue
-            xs = x[:Ts].contiguous()
-            lgs = torch.from_numpy(gen_logits(c.get("seed", 0) + rank, Ts, E)).to(dev)
-            os_ = torch.empty((Ts, H), dtype=torch.bfloat16, device=dev)
-            for _ in range(3):
-                m.forward(lgs, xs, k, out=os_)
-            ev = []
-            for _ in range(max(10, args.steps)):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                m.forward(lgs, xs, k, out=os_)
-                b.record(stream)
-                ev.append((a, b))
-            torch.cuda.synchronize()
-            ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-            sweep[str(Ts)] = {"tokens_per_s": Ts / (ms / 1e3), "ms": ms}
+            Ls = make_layer(**{**c, "T": Ts, "seed": c.get("seed", 0) + rank})
+            r = measure_layer(Ls, dev, max(20, args.steps // 2), 3, flush, stream, None, e2e=False)
+            sweep[str(Ts)] = {"tokens_per_s": Ts / (np.mean(r["step_ms"]) / 1e3),
+                              "ms": float(np.mean(r["step_ms"])),
+                              "ffn_hbm_frac": ffn_roofline(Ls, r["U"], r["ffn_ms"], pk, pk_kind, "")["frac"]}
+
+    # ---- the compute-bound prefill layer (same shape, 4096 tokens), Q4_0 and MXFP4
+    prefill = None
+    if not args.no_prefill and args.config == "decode":
+        prefill = {}
+        for qt in CONFIGS["prefill"]["qtypes"]:
+            cp = dict(CONFIGS["prefill"])
+            cp["qtype"] = qt
+            Lp = make_layer(**{**cp, "seed": cp.get("seed", 0) + rank})
+            r = measure_layer(Lp, dev, max(10, args.steps // 10), 3, flush, stream, None, e2e=False)
+            wl = f"prefill layer H{Lp.H} I{Lp.I} E{Lp.E} top-{Lp.k} {qt} T{Lp.T}"
+            prefill[qt] = {"workload": wl, "tokens_per_s": Lp.T / (np.mean(r["step_ms"]) / 1e3),
+                           "ms_per_step": float(np.mean(r["step_ms"])),
+                           "roofline": ffn_roofline(Lp, r["U"], r["ffn_ms"], pk, pk_kind, wl)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -355,28 +260,153 @@ def main():
         cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"one oracle layer pass over {sample_T} tokens of the workload ({dt:.1f} s)"}
 
-    launches_per_step = 1 + (1 if P <= 16384 else 3) + 2 + 1
+    launches_per_step = 1 + (1 if P <= 16384 else 3) + 2 + 1 + (2 if L.shared_w13 is not None else 0)
     if rank == 0:
         line = {
             "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(step_ms)),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(head["step_ms"])),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
-            "config": {"workload": cfg["workload"], "H": L.H, "I": L.I, "E": L.E, "k": k, "T": T,
+            "config": {"workload": cfg["workload"], "H": H, "I": I, "E": E, "k": k, "T": T,
                        "qtype": L.qtype, "parallelism": f"replicas{world}",
                        "l2": "flushed between steps (512 MB write)"},
             "roofline": roofline,
-            "layer_hbm_frac": layer_frac,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "decode_sweep": sweep or None,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload):
+    """Roofline of the expert FFN step (its two launches).  Few rows per expert: HBM-bound
+    grouped GEMV, algorithmic bytes = the selected experts' weights + activation rows.  Many
+    rows per expert: tensor-bound grouped GEMM, algorithmic flops = 2 * P * 3 * H * I."""
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
+    P = T * k
+    gemm = P >= 32 * E  # the library's automatic path choice
+    if not gemm:
+        blob = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
+        alg = U * blob + P * H * 2 + P * H * 2 + T * H * 2 + P * I * 2 * 2
+        hbm = float(pk["hbm_gbs"])
+        ach = alg / (ffn_ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "gemv_ffn_kernel x2 (gate/up+SwiGLU, down)",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_kind": f"{pk_kind} hbm_gbs (copy)",
+                "traffic": recorded_traffic("expert_ffn_gemv", workload),
+                "alg_bytes_per_launch": alg, "ms_per_launch": ffn_ms, "unique_experts": U}
+    flops = 2.0 * P * 3 * H * I
+    peak = float(pk["bf16_tflops"])
+    ach = flops / (ffn_ms / 1e3) / 1e12
+    return {"bound": "tensor", "kernel": "gemm_ffn_kernel x2 (tcgen05 kind::f16; gate/up+SwiGLU, down)",
+            "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+            "peak_kind": f"{pk_kind} bf16_tflops (burst; the FFN is timed alone)",
+            "traffic": recorded_traffic("expert_ffn_gemm", workload),
+            "alg_flops_per_launch": flops, "ms_per_launch": ffn_ms, "unique_experts": U}
+
+
+def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
+    """Times `steps` layer steps (L2 flushed between steps, outside the events), then the
+    expert-FFN step alone, then (e2e) the step with host<->device copies inside the events."""
+    import torch
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev)
+    T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
+    P = T * k
+    x = torch.from_numpy(L.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(L.logits).to(dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+
+    def timed(fn, n):
+        ev = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def step():
+        m.forward(lg, x, k, out=out, ids_out=ids, w_out=wts)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    U = unique_experts(ids.cpu().numpy())
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    if clk is not None:  # clocks sampled during the timed region only
+        with clk:
+            step_ms = timed(step, steps)
+    else:
+        step_ms = timed(step, steps)
+    if pg:
+        pg.barrier()
+    my_ms = float(np.sum(step_ms))
+    max_ms = my_ms
+    if pg:
+        t = torch.tensor([my_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    # the expert FFN alone (its two launches), inputs from this routing
+    ws_n = F.ftmoe_ffn_workspace_bytes(T, k, E, H, I)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    inv = torch.empty(P, dtype=torch.int32, device=dev)
+    pws_n = F.ftmoe_permute_workspace_bytes(T, k, E)
+    pws = torch.empty(max(pws_n, 256), dtype=torch.uint8, device=dev)
+    F.ftmoe_permute(ids, T, k, E, offs, sp, inv, pws, pws_n)
+    y_perm = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
+
+    def ffn():
+        F.ftmoe_expert_ffn(m.weights, x, T, k, offs, sp, y_perm, ws, ws_n)
+
+    for _ in range(3):
+        ffn()
+    ffn_ms = float(np.mean(timed(ffn, steps)))
+
+    res = {"U": U, "step_ms": step_ms, "max_ms": max_ms, "ffn_ms": ffn_ms}
+    if e2e:
+        # end to end through the C ABI with pinned host buffers, copies inside the events
+        x_h = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        lg_h = torch.from_numpy(L.logits).pin_memory()
+        out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        x_d = torch.empty_like(x)
+        lg_d = torch.empty_like(lg)
+
+        def e2e_step():
+            x_d.copy_(x_h, non_blocking=True)
+            lg_d.copy_(lg_h, non_blocking=True)
+            m.forward(lg_d, x_d, k, out=out)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = float(np.sum(timed(e2e_step, steps)))
+        e2e_max = e2e_ms
+        if pg:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_max = float(t.item())
+        res["e2e_max_ms"] = e2e_max
+    return res
 
 
 if __name__ == "__main__":

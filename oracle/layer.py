@@ -45,20 +45,19 @@ def layer_rows(x_bits, logits, k, qtype, w13, w2, rows, shared_w13=None, shared_
 
     A token's output depends only on its own activations and logits:
     out[t] = sum_j w[t, j] * FFN_{ids[t, j]}(x[t]) (+ FFN_shared(x[t])).
+    The experts are visited one at a time (decoded once, applied to every sampled token
+    that selected it) so that only one expert's fp64 weights are held at a time.
     Returns (ids [n, k], w [n, k], out fp64 [n, H]) for the tokens in ``rows``."""
     rows = np.asarray(rows, dtype=np.int64)
     x = _x_fp64(np.asarray(x_bits)[rows])
     ids, w = route(np.asarray(logits)[rows], k)
     n, H = x.shape
     out = np.zeros((n, H))
-    cache13, cache2 = {}, {}
-    for i in range(n):
-        for j in range(k):
-            e = int(ids[i, j])
-            if e not in cache13:
-                cache13[e] = decode_blocks(w13[e], qtype)
-                cache2[e] = decode_blocks(w2[e], qtype)
-            out[i] += w[i, j] * swiglu_ffn(x[i:i + 1], cache13[e], cache2[e])[0]
+    for e in np.unique(ids):
+        sel_i, sel_j = np.nonzero(ids == e)
+        y = swiglu_ffn(x[sel_i], decode_blocks(w13[e], qtype), decode_blocks(w2[e], qtype))
+        for r, (i, j) in enumerate(zip(sel_i, sel_j)):
+            out[i] += w[i, j] * y[r]
     if shared_w13 is not None:
         out += swiglu_ffn(x, decode_blocks(shared_w13[0], qtype), decode_blocks(shared_w2[0], qtype))
     return ids, w, out

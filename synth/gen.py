@@ -125,7 +125,11 @@ def quantize_mxfp4(w: np.ndarray) -> np.ndarray:
     K = w.shape[-1]
     assert K % BLOCK == 0
     lead = w.shape[:-1]
-    b = w.reshape(-1, BLOCK).astype(np.float64)
+    flat = w.reshape(-1, BLOCK)
+    if flat.shape[0] > (1 << 18):  # bound the temporaries: encode in slices of blocks
+        parts = [quantize_mxfp4(flat[i:i + (1 << 18)]) for i in range(0, flat.shape[0], 1 << 18)]
+        return np.concatenate(parts, axis=0).reshape(*lead, K // BLOCK, 17)
+    b = flat.astype(np.float64)
     n = b.shape[0]
     amax = np.max(np.abs(b), axis=1)
     with np.errstate(divide="ignore"):

@@ -1,0 +1,115 @@
+"""Expert cache on the GPU: a pinned-host expert bank streamed into a device slot pool.
+
+The slot choice of every prefetch / acquire must equal the CPU LRU simulator's
+exactly (same hits, misses and slots), the resident slot bytes must equal the bank
+bytes, and a layer computed from the cache slots (a per-expert pointer table) must
+give the same bits as the same layer computed from contiguous weights.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import make_layer, stream_trace
+from tests._util import bf16_tensor, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+LAYERS, E, K, H, I, SLOTS = 3, 8, 2, 256, 128, 3
+
+
+@pytest.fixture(scope="module")
+def env(cuda_device):
+    ensure_built()
+    import torch
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    return F, torch, cuda_device
+
+
+def _bank(env, qtype):
+    """Per layer: the layer inputs, its device weights (MoELayer) and its expert blobs."""
+    F, torch, dev = env
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    layers = []
+    for l in range(LAYERS):
+        L = make_layer(H=H, I=I, E=E, k=K, T=1, qtype=qtype, seed=100 + l)
+        m = MoELayer(qtype, E, H, I, L.w13, L.w2, device=dev)
+        blobs = torch.cat([m.w13.view(E, -1), m.w2.view(E, -1)], dim=1).contiguous()
+        layers.append((L, m, blobs))
+    nb = layers[0][2].shape[1]
+    assert nb == F.ftmoe_expert_blob_bytes(qtype, H, I)
+    bank = torch.empty((LAYERS, E, nb), dtype=torch.uint8).pin_memory()
+    for l, (_, _, blobs) in enumerate(layers):
+        bank[l].copy_(blobs.cpu())
+    return layers, bank, nb
+
+
+@pytest.mark.parametrize("policy", ["layer", "global"])
+def test_cache_matches_lru_simulator_and_contiguous_layer(env, policy):
+    F, torch, dev = env
+    layers, bank, nb = _bank(env, "q4_0")
+    pool = torch.zeros(LAYERS * SLOTS * nb, dtype=torch.uint8, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    compute = torch.cuda.current_stream(dev)
+    pol = F.LRU_PER_LAYER if policy == "layer" else F.LRU_GLOBAL
+    cache = F.ExpertCache(LAYERS, E, nb, bank, pool, SLOTS, pol, copy_stream)
+    sim = oracle.LRUSim(LAYERS, E, SLOTS, policy)
+    steps = 12
+    trace = stream_trace(7, steps, LAYERS, E, K, p_repeat=0.5, s=1.0)
+    misses = hits = 0
+    for st in range(steps):
+        # prefetch layer 0 of the step, then per layer: prefetch the next, acquire this one
+        pslots, pcopied = cache.prefetch(0, trace[st, 0])
+        want = sim.request(0, trace[st, 0])
+        assert [s for s, _ in want] == pslots and [c for _, c in want] == pcopied
+        for l in range(LAYERS):
+            if l + 1 < LAYERS:
+                pslots, pcopied = cache.prefetch(l + 1, trace[st, l + 1])
+                want = sim.request(l + 1, trace[st, l + 1])
+                assert [s for s, _ in want] == pslots and [c for _, c in want] == pcopied
+            blob_ptrs, slots, copied = cache.acquire(l, trace[st, l], compute)
+            want = sim.request(l, trace[st, l])
+            assert [s for s, _ in want] == slots and [c for _, c in want] == copied
+            misses += sum(copied)
+            hits += len(copied) - sum(copied)
+            # the layer on one token whose routing picks exactly the acquired experts
+            L, m, _ = layers[l]
+            logits = np.full((1, E), -4.0, dtype=np.float32)
+            logits[0, trace[st, l, 0]] = 2.0
+            logits[0, trace[st, l, 1]] = 1.0
+            lg = torch.from_numpy(logits).to(dev)
+            x = bf16_tensor(L.x, dev)
+            table = [blob_ptrs[e] if e in set(int(v) for v in trace[st, l]) else None for e in range(E)]
+            wt = F.make_weights("q4_0", E, H, I, expert_blob=table)
+            ws = m.workspace(1, K)
+            out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+            F.ftmoe_layer(wt, lg, x, 1, K, out, None, None, ws, ws.numel())
+            cache.release(l, compute)
+            ref = m.forward(lg, x, K)
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (st, l)
+    stats = cache.stats()
+    assert stats["misses"] == misses and stats["hits"] == hits
+    assert stats["lookups"] == steps * LAYERS * K
+    assert stats["h2d_bytes"] == nb * (stats["misses"] + stats["prefetch_copies"])
+    # every resident slot holds exactly its expert's bank bytes
+    torch.cuda.synchronize()
+    pool_h = pool.view(-1, nb).cpu()
+    nslot = SLOTS if policy == "layer" else SLOTS * LAYERS
+    for (l, e), s in sim.where.items():
+        gs = (l * nslot + s) if policy == "layer" else s
+        assert torch.equal(pool_h[gs], bank[l, e]), (l, e, s)
+    cache.close()
+
+
+def test_cache_rejects_requests_larger_than_the_pool(env):
+    F, torch, dev = env
+    layers, bank, nb = _bank(env, "mxfp4")
+    pool = torch.zeros(LAYERS * SLOTS * nb, dtype=torch.uint8, device=dev)
+    cache = F.ExpertCache(LAYERS, E, nb, bank, pool, SLOTS, F.LRU_PER_LAYER, torch.cuda.Stream(dev))
+    with pytest.raises(F.FtmoeError) as ei:
+        cache.prefetch(0, [0, 1, 2, 3])  # 4 ids, 3 slots
+    assert ei.value.status == 4  # FTMOE_ERR_NO_SLOT
+    with pytest.raises(F.FtmoeError) as ei:
+        cache.prefetch(0, [0, E])  # expert id out of range
+    assert ei.value.status == 1
+    cache.close()

@@ -265,11 +265,13 @@ def main():
         line = {
             "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(head["step_ms"])),
+            "eager_ms_per_step": head["eager_ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
             "config": {"workload": cfg["workload"], "H": H, "I": I, "E": E, "k": k, "T": T,
                        "qtype": L.qtype, "parallelism": f"replicas{world}",
-                       "l2": "flushed between steps (512 MB write)"},
+                       "l2": "flushed between steps (512 MB write)",
+                       "step": "whole layer replayed from a CUDA graph"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
@@ -346,14 +348,20 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
         step()
     torch.cuda.synchronize()
     U = unique_experts(ids.cpu().numpy())
+    eager_ms = timed(step, steps)  # one launch per kernel from the host, for reference
+    # the timed step: the whole layer replayed from a CUDA graph
+    graph = m.capture(step)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     if clk is not None:  # clocks sampled during the timed region only
         with clk:
-            step_ms = timed(step, steps)
+            step_ms = timed(graph.replay, steps)
     else:
-        step_ms = timed(step, steps)
+        step_ms = timed(graph.replay, steps)
     if pg:
         pg.barrier()
     my_ms = float(np.sum(step_ms))
@@ -381,7 +389,8 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
         ffn()
     ffn_ms = float(np.mean(timed(ffn, steps)))
 
-    res = {"U": U, "step_ms": step_ms, "max_ms": max_ms, "ffn_ms": ffn_ms}
+    res = {"U": U, "step_ms": step_ms, "max_ms": max_ms, "ffn_ms": ffn_ms,
+           "eager_ms": float(np.mean(eager_ms))}
     if e2e:
         # end to end through the C ABI with pinned host buffers, copies inside the events
         x_h = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -399,7 +408,11 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
-        e2e_ms = float(np.sum(timed(e2e_step, steps)))
+        e2e_graph = m.capture(e2e_step)  # copies in, layer, copy out: one graph launch
+        for _ in range(3):
+            e2e_graph.replay()
+        torch.cuda.synchronize()
+        e2e_ms = float(np.sum(timed(e2e_graph.replay, steps)))
         e2e_max = e2e_ms
         if pg:
             t = torch.tensor([e2e_ms], device=dev)

@@ -704,7 +704,7 @@ static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
   auto kern = gemm_ffn_kernel<QT, MODE, Tab>;
   constexpr size_t smem = gm_smem_bytes<MODE>();
   static_assert(smem <= 232448, "shared memory per CTA");
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = set_smem_limit<gemm_ffn_kernel<QT, MODE, Tab>>(smem);
   if (err != cudaSuccess) return err;
   kern<<<di->sm_count, GM_THREADS, smem, st>>>(a, tab, map);
   return cudaGetLastError();

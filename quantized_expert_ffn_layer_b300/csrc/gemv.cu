@@ -400,6 +400,7 @@ static int pick_kp(int T, long long units, int NP, int sm_count) {
   const long long want = 2LL * sm_count * 2 * GW_WARPS;
   int kp = 1;
   while (kp < GW_KPMAX && units * kp < want && 2 * kp <= NP) kp *= 2;
+  if (kp < NP && units * kp < want / 2) kp = NP < GW_KPMAX ? NP : GW_KPMAX;  // one part per warp
   return kp;
 }
 
@@ -438,7 +439,7 @@ static cudaError_t launch_mode(const GemvArgs& a, const Tab& tab, int max_active
   if (!di) return cudaErrorUnknown;
   auto kern = gemv_ffn_kernel<QT, MODE, Tab>;
   const size_t smem = sizeof(GwSmem<QT>);
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = set_smem_limit<gemv_ffn_kernel<QT, MODE, Tab>>(smem);
   if (err != cudaSuccess) return err;
   const long long items = (long long)max_active * a.units_per_expert * a.kp;
   long long grid = (items + GW_WARPS - 1) / GW_WARPS;

@@ -16,6 +16,20 @@ struct DeviceInfo {
 };
 const DeviceInfo* device_info();  // for the current device; nullptr on failure
 
+// Raises kernel K's dynamic shared-memory limit on the current device the first time it
+// is needed; later calls with no larger size return at once (no driver call, so the
+// launch paths stay cheap and can be recorded into CUDA graphs).
+template <auto K>
+cudaError_t set_smem_limit(size_t bytes) {
+  static int done[64] = {0};  // bytes granted so far, per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE) >= (int)bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) __atomic_store_n(&done[dev], (int)bytes, __ATOMIC_RELEASE);
+  return e;
+}
+
 cudaError_t launch_repack(int qtype, const void* canon, void* tiles, int E, int N, int K,
                           cudaStream_t st);
 cudaError_t launch_dequant(int qtype, const void* tiles, int E, int N, int K, float* out,

@@ -205,8 +205,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   const int zero_n = zero_ptr ? (int)(zero_bytes / 4) : 0;
   if (P <= PSMALL_MAX) {
     const size_t smem = (size_t)(35 * E + 32) * sizeof(int);
-    cudaError_t err = cudaFuncSetAttribute(permute_small_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = set_smem_limit<permute_small_kernel>(smem);
     if (err != cudaSuccess) return err;
     permute_small_kernel<<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status,
                                                 (int*)zero_ptr, zero_n);
@@ -218,8 +217,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
                                                                (int*)zero_ptr, zero_n);
   permute_scan_kernel<<<1, PCHUNK, 0, st>>>(hist, nchunk, E, offsets);
   const size_t smem = (size_t)33 * E * sizeof(int);
-  cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = set_smem_limit<permute_scatter_kernel>(smem);
   if (err != cudaSuccess) return err;
   permute_scatter_kernel<<<nchunk, PCHUNK, smem, st>>>(ids, P, E, hist, sorted_pair, inv_pos);
   return cudaGetLastError();

@@ -39,6 +39,21 @@ class MoELayer:
             self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws
 
+    def capture(self, fn):
+        """Records fn() (calls of this layer and any stream-ordered copies around them) into a
+        CUDA graph and returns it: graph.replay() reruns every kernel and copy of fn on the
+        same buffers with one launch.  fn runs once first, outside the capture, so that the
+        kernels' one-time settings are made before recording."""
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        return g
+
     def forward(self, logits, x_bf16, k, out=None, ids_out=None, w_out=None, stream=None):
         """logits fp32 [T, E], x bf16 [T, H] (device) -> out bf16 [T, H]."""
         T = x_bf16.shape[0]

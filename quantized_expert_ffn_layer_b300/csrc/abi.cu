@@ -111,13 +111,18 @@ ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, 
   FfnWs fw = carve_ffn(ws, T, k, E, wts->H, wts->I);
   pb.h_act = fw.h_act;
   const int path = g_ffn_path;
-  const bool want_gemm =
-      path == FTMOE_PATH_GEMM || (path == FTMOE_PATH_AUTO && (long long)pb.P >= 32LL * E);
-  if (want_gemm) {
+  const bool many_rows = (long long)pb.P >= 32LL * E;
+  if (path == FTMOE_PATH_GEMM || (path == FTMOE_PATH_AUTO && many_rows)) {
     cudaError_t e = launch_ffn_gemm(pb, fw.gemm_ws, fw.gemm_bytes, st);
     if (e == cudaSuccess) return FTMOE_OK;
     if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
     if (path == FTMOE_PATH_GEMM) return FTMOE_ERR_UNSUPPORTED;
+  }
+  if (path == FTMOE_PATH_GEMM_DECODE) {
+    cudaError_t e = launch_ffn_gemm_decode(pb, st);
+    if (e == cudaSuccess) return FTMOE_OK;
+    if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
+    return FTMOE_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_ffn_gemv(pb, fw.gemv_ws, ws_zeroed, st));
 }
@@ -208,7 +213,7 @@ size_t ftmoe_ffn_workspace_bytes(int T, int k, int E, int H, int I) {
 
 int ftmoe_set_ffn_path(int path) {
   const int old = g_ffn_path;
-  if (path >= FTMOE_PATH_AUTO && path <= FTMOE_PATH_GEMM) g_ffn_path = path;
+  if (path >= FTMOE_PATH_AUTO && path <= FTMOE_PATH_GEMM_DECODE) g_ffn_path = path;
   return old;
 }
 

@@ -1,0 +1,664 @@
+// Grouped expert FFN on the 5th-generation tensor cores for few rows per expert
+// (decode): the ExpertFFN of the FreeToken architecture walkthrough §五 on its GGUF
+// Q4_0 / MXFP4 banks, with the block decode of §六 done by the SM into tensor memory.
+//
+// Decode reads every selected expert's weights once for a handful of tokens, so the
+// layer is bound by streaming the 4-bit weights from HBM.  One persistent CTA per SM
+// works through items (expert, 128 weight rows, up to 32 of the expert's token rows):
+// for gate/up the gate and the up rows of 128 features (two A tiles), for down one
+// 128-row tile.  Per 64-element reduction block ("stage"):
+//   * a raw-weight warp keeps a deep ring of shared-memory slots filled with the
+//     stage's 4-bit weight records (1-D bulk copies) and warms L2 with the next item;
+//   * 16 converter warps decode the records into exact bf16 (round-to-nearest-even of
+//     the decoded value); each thread owns one weight row (its tensor-memory lane) and
+//     writes its columns of the A tile with tcgen05.st; they also gather the item's
+//     token rows (x for gate/up through the permutation, h for down) with cp.async
+//     into the 128-byte-swizzled K-major B tile;
+//   * one thread issues tcgen05.mma kind::f16 with A from tensor memory and B from
+//     shared memory (M = 128, N = the token count rounded up to 16, K = 16);
+//   * 4 epilogue warps read the accumulators with tcgen05.ld (two buffers, so the
+//     epilogue of one item overlaps the MMAs of the next) and store h = silu(g) * u or
+//     y as bf16.
+// The multiply-accumulate order over the reduction dimension is fixed and each output
+// depends only on its own weight row and token row, so a token's result does not
+// depend on the other tokens of the batch.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "pipeline.cuh"
+#include "tcgen05.cuh"
+
+namespace ftmoe {
+namespace dec {
+
+constexpr int GD_TOK = 32;          // token rows per item (largest MMA N)
+constexpr int GD_ROWS = 128;        // weight rows per tile (MMA M, TMEM lanes)
+constexpr int GD_EPI_WARPS = 4;     // warps 0..3 (one per TMEM lane quarter)
+constexpr int GD_MMA_WARP = 4;      // TMEM owner; lane 0 issues the MMAs
+constexpr int GD_RAW_WARP = 5;      // bulk copies of the raw weight records; warps 6, 7 idle
+constexpr int GD_CONV0 = 8;         // first converter warp (a multiple of 4)
+constexpr int GD_CONV_WARPS = 16;
+constexpr int GD_CONV_THREADS = GD_CONV_WARPS * 32;
+constexpr int GD_THREADS = (GD_CONV0 + GD_CONV_WARPS) * 32;  // 768
+constexpr uint32_t GD_TMEM_COLS = 512;
+constexpr int GD_B_TILE = GD_TOK * 128;   // 4 KB of bf16 (32 token rows x 64)
+constexpr int GD_ECOL = 16;               // accumulator columns (tokens) per epilogue step
+constexpr int GD_STG = GD_ECOL * 64;      // epilogue staging per warp: 16 rows x 32 bf16
+constexpr int GD_MAX_E = 1024;
+constexpr int GD_MAX_NR = 16;
+constexpr int GD_MAX_NS = 8;
+
+// Per-projection layout.  Tensor-memory columns: two accumulator buffers of NT x 32
+// columns, then NS stages of A tiles (NT x 32 columns: 64 bf16 per lane).  The raw
+// weight ring (shared memory) holds super-stages of NKB consecutive k-blocks, filled
+// with one bulk copy per record row group (records of a row group are contiguous along
+// the reduction dimension), so that enough HBM reads are in flight with few copy ops.
+template <int MODE>
+struct GdCfg {
+  static constexpr int NT = MODE == 0 ? 2 : 1;            // A tiles (MMAs per k-step)
+  static constexpr int NACC = 2;                          // accumulator buffers
+  static constexpr int NS = MODE == 0 ? 6 : 8;            // A / B stages
+  static constexpr int LA = NS - 3;                       // token-row copy stages in flight
+  static constexpr int NKB = 4;                           // k-blocks per raw super-stage
+  static constexpr int NR = MODE == 0 ? 3 : 4;            // raw weight super-stages
+  static constexpr int NREC = 8 * NT;                     // weight records per stage
+  static constexpr int RAW_STAGE = NREC * NKB * 576;      // [record][k-block][576]
+  static constexpr int ACC_COLS = NT * GD_TOK;            // columns of one accumulator buffer
+  static constexpr int A_COL0 = NACC * ACC_COLS;          // first A-stage column
+  static constexpr int A_STAGE_COLS = NT * 32;
+  static_assert(A_COL0 + NS * A_STAGE_COLS <= (int)GD_TMEM_COLS, "tensor memory columns");
+  static_assert(NS <= GD_MAX_NS && NR <= GD_MAX_NR && LA >= 1, "ring sizes");
+  // converter threads: one weight row each (its TMEM lane), covering 64 / CPR
+  // reduction elements of the stage (CPR = converter threads per row)
+  static constexpr int CPR = GD_CONV_THREADS / (NT * GD_ROWS);
+  static constexpr int NSTEP = 4 / CPR;                   // 16-element steps per thread
+};
+
+struct GdTail {
+  uint64_t raw_full[GD_MAX_NR], raw_empty[GD_MAX_NR];
+  uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS];
+  uint64_t acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int citem[GD_MAX_E + 1];  // exclusive prefix of items per expert
+};
+template <int MODE>
+constexpr size_t gd_smem_bytes() {
+  return 1024 + (size_t)GdCfg<MODE>::NS * GD_B_TILE + (size_t)GdCfg<MODE>::NR * GdCfg<MODE>::RAW_STAGE +
+         (size_t)GD_EPI_WARPS * GD_STG + sizeof(GdTail);
+}
+
+struct GemmArgs {
+  const int32_t* offsets;
+  const int32_t* sorted_pair;  // gate/up: pair of each permuted row (nullptr: identity)
+  int k, E;
+  const uint16_t* act;  // gate/up: x [T][H] (rows gathered); down: h [P][I] (contiguous rows)
+  int act_ld;
+  uint16_t* out;        // gate/up: h [P][I]; down: y_perm [P][H]
+  int out_ld;
+  const uint8_t* wbase;  // tiles of this projection for expert 0
+  long long wstride;     // bytes between experts
+  long long table_off;   // offset of this projection inside a blob
+  int S;                 // 64-element reduction blocks (records per 16-row group)
+  int K;                 // reduction length
+  int nrows;             // output rows of the projection's result: I or H
+  int up_row0;           // gate/up: first up row of w13 (= I)
+  int ft_per_expert;     // weight-row slices per token tile
+  int* status;
+};
+
+struct GmNoTable {
+  __device__ __forceinline__ const uint8_t* get(int e, const GemmArgs& a) const {
+    return a.wbase + (long long)e * a.wstride;
+  }
+};
+struct GmWithTable {
+  ExpertTable t;
+  __device__ __forceinline__ const uint8_t* get(int e, const GemmArgs& a) const {
+    return t.p[e] + a.table_off;
+  }
+};
+
+struct GmItem {
+  int e, r0, n, f0;
+};
+
+template <int MODE>
+__device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* citem) {
+  int lo = 0, hi = a.E;  // largest e with citem[e] <= i (that expert has items)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (citem[mid] <= i) lo = mid; else hi = mid;
+  }
+  GmItem it;
+  it.e = lo;
+  const int local = i - citem[lo];
+  const int beg = a.offsets[lo], ne = a.offsets[lo + 1] - beg;
+  const int ntt = (ne + GD_TOK - 1) / GD_TOK;
+  const int ft = local / ntt, tt = local - ft * ntt;
+  it.r0 = beg + tt * GD_TOK;
+  it.n = min(GD_TOK, ne - tt * GD_TOK);
+  it.f0 = ft * GD_ROWS;
+  return it;
+}
+
+// First matrix row of record ri (tile ri / 8, 16-row group ri % 8) of an item, and
+// whether that row group lies inside the projection's result rows.
+template <int MODE>
+__device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const GemmArgs& a,
+                                             bool& ok) {
+  const int row = it.f0 + (ri & 7) * 16;
+  ok = row < a.nrows;
+  return (MODE == 0 && (ri >> 3)) ? row + a.up_row0 : row;
+}
+
+// ---------------------------------------------------------------- weight decode
+// Block scale of one row as (hi, lo) bf16x2 pairs with hi + lo == the scale exactly
+// (Q4_0 fp16 d), or (2^(e-127), 0) for an MXFP4 E8M0 byte.
+template <int QT>
+__device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
+  if (QT == FTMOE_Q4_0) {
+    const float d = half_bits_to_f32(bits);
+    const uint32_t hi = f32_to_bf16_bits(d);
+    const uint32_t lo = f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
+    hi2 = hi | (hi << 16);
+    lo2 = lo | (lo << 16);
+  } else {
+    const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
+    hi2 = b | (b << 16);
+    lo2 = 0;
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t saddr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
+  return v;
+}
+
+// Two bf16x2 pairs (elements 0,1 and 2,3 of a 4-element group) from a nibble word E whose
+// bytes hold the group's codes in the order (e0, e2, e1, e3), each in the low nibble.
+template <int QT>
+__device__ __forceinline__ void decode_group(uint32_t E, uint32_t s_hi, uint32_t s_lo, uint32_t& o0,
+                                             uint32_t& o1) {
+  if (QT == FTMOE_Q4_0) {
+    const uint32_t K = 0x43434343u;  // high byte of bf16 128: (128 + q) per element
+    const uint32_t t[2] = {prmt(E, K, 0x4240u), prmt(E, K, 0x4341u)};
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+    uint32_t r[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      // RNE((q - 8) * d) with d = hi + lo split exactly
+      const __nv_bfloat162 u = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t[p]), off);
+      const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
+      const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
+      r[p] = *reinterpret_cast<const uint32_t*>(&w);
+    }
+    o0 = r[0];
+    o1 = r[1];
+  } else {
+    const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
+    const uint32_t TWO126 = 0x7E807E80u;
+    uint32_t r[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      uint32_t t = ((v[p] & 0x00070007u) << 6) | ((v[p] & 0x00080008u) << 12);  // E2M1 * 2^-126
+      __nv_bfloat162 w = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&t),
+                                 *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
+      w = __hmul2(w, *reinterpret_cast<const __nv_bfloat162*>(&s_hi));
+      r[p] = *reinterpret_cast<const uint32_t*>(&w);
+    }
+    o0 = r[0];
+    o1 = r[1];
+  }
+}
+
+// One converter thread decodes NSTEP 16-element steps (from J0) of one weight row and
+// writes them to its tensor-memory lane.  The row is row g + 8 h of a record in shared
+// memory; record lane 4g + c holds, in word j, elements 16j + 4c + (0..3) of rows g and
+// g + 8 (row g in nibble slots 0,4,2,6, row g + 8 in slots 1,5,3,7).  The four segment
+// loads are issued in an order rotated by (g >> 1) so that the 8 rows g of a record read
+// 8 different bank groups, then put back in segment order.
+template <int QT, int NSTEP>
+__device__ __forceinline__ void convert_row(uint32_t rec, uint32_t taddr, int g, int h, int j0) {
+  const int rot = (g >> 1) & 3;
+  uint32_t w[4][NSTEP];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t addr = rec + (4 * g + ((i + rot) & 3)) * 16 + 4 * j0;
+    if constexpr (NSTEP == 2) {
+      const uint2 v = lds64(addr);
+      w[i][0] = v.x;
+      w[i][NSTEP - 1] = v.y;
+    } else {
+      w[i][0] = lds32(addr);
+    }
+  }
+  // v[c] = w[(c - rot) & 3]
+  uint32_t v[4][NSTEP];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int s = 0; s < NSTEP; ++s) {
+      const uint32_t x0 = w[c][s], x1 = w[(c + 3) & 3][s], x2 = w[(c + 2) & 3][s], x3 = w[(c + 1) & 3][s];
+      v[c][s] = rot == 0 ? x0 : rot == 1 ? x1 : rot == 2 ? x2 : x3;
+    }
+  // block scale of this row
+  uint32_t sh, sl;
+  {
+    const int idx = (g * 2 + (j0 >> 1)) * 2 + h;
+    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
+    const uint32_t wd = lds32(rec + REC_CODE_BYTES + (byte & ~3));
+    const uint32_t bits = QT == FTMOE_Q4_0 ? (wd >> (8 * (byte & 3))) & 0xFFFFu
+                                           : (wd >> (8 * (byte & 3))) & 0xFFu;
+    row_scale<QT>(bits, sh, sl);
+  }
+  uint32_t out[8 * NSTEP];
+  const int hs = 4 * h;
+#pragma unroll
+  for (int s = 0; s < NSTEP; ++s)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      decode_group<QT>((v[c][s] >> hs) & 0x0F0F0F0Fu, sh, sl, out[8 * s + 2 * c], out[8 * s + 2 * c + 1]);
+  if constexpr (NSTEP == 2) tmem_st16(taddr, out);
+  else tmem_st8(taddr, out);
+}
+
+// 16-byte global -> shared copy (LDGSTS); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Brings [p, p + bytes) into L2 ahead of use (bytes % 16 == 0, p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+template <int QT, int MODE, class Tab>
+__global__ void __launch_bounds__(GD_THREADS, 1)
+    gemm_decode_kernel(const GemmArgs a, const __grid_constant__ Tab tab) {
+  using C = GdCfg<MODE>;
+  constexpr int RB = rec_bytes(QT);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // B stages (128-byte swizzle)
+  uint8_t* base = smem_raw + (base_addr - raw_addr);
+  const uint32_t rawring = base_addr + C::NS * GD_B_TILE;
+  const uint32_t staging = rawring + C::NR * C::RAW_STAGE;
+  GdTail& tl = *reinterpret_cast<GdTail*>(base + (size_t)C::NS * GD_B_TILE +
+                                          (size_t)C::NR * C::RAW_STAGE + GD_EPI_WARPS * GD_STG);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &tl.abort_flag;
+
+  if (MODE == 0) pdl_wait();  // offsets come from the permutation kernel
+  if (tid == 0) {
+    for (int s = 0; s < C::NR; ++s) {
+      mbar_init(&tl.raw_full[s], 1);
+      mbar_init(&tl.raw_empty[s], GD_CONV_WARPS);
+    }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&tl.a_full[s], GD_CONV_WARPS);
+      mbar_init(&tl.empty[s], 1);
+    }
+    for (int b = 0; b < C::NACC; ++b) {
+      mbar_init(&tl.acc_full[b], 1);
+      mbar_init(&tl.acc_empty[b], GD_EPI_WARPS * 32);
+    }
+    mbar_init(&tl.drain, 1);
+    tl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == GD_MMA_WARP) {
+    tmem_alloc(&tl.tmem_base, GD_TMEM_COLS);
+    tmem_relinquish();
+  }
+  // items per expert: ceil(n_e / 32) token tiles x weight-row slices
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+      const int e = e0 + lane;
+      int v = 0;
+      if (e < a.E) v = ((a.offsets[e + 1] - a.offsets[e] + GD_TOK - 1) / GD_TOK) * a.ft_per_expert;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (e < a.E) tl.citem[e] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) tl.citem[a.E] = carry;
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  pdl_launch_dependents();
+  const uint32_t tmem = tl.tmem_base;
+  const int nitems = tl.citem[a.E];
+  const int G = gridDim.x;
+
+  if (warp == GD_RAW_WARP) {
+    // ------------------------------------------------------------ raw weight records
+    int rslot = 0;
+    uint32_t rphase = 0;
+    for (int i = blockIdx.x; i < nitems; i += G) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      // lane r < NREC: record r of every stage (tile r / 8, row group r % 8)
+      bool rok = false;
+      const uint8_t* rec0 = nullptr;
+      if (lane < C::NREC)
+        rec0 = tab.get(it.e, a) + (long long)(gm_record_row<MODE>(it, lane, a, rok) / 16) * a.S * RB;
+      const int nrec = __popc(__ballot_sync(0xffffffffu, lane < C::NREC && rok));
+      // warm L2 with the CTA's next item's records while this one streams
+      if (i + G < nitems && lane < C::NREC) {
+        const GmItem nx = gm_item<MODE>(i + G, a, tl.citem);
+        bool nok;
+        const int nrow = gm_record_row<MODE>(nx, lane, a, nok);
+        if (nok) prefetch_l2(tab.get(nx.e, a) + (long long)(nrow / 16) * a.S * RB, (uint32_t)(a.S * RB));
+      }
+      for (int kb0 = 0; kb0 < a.S; kb0 += C::NKB) {
+        const int nkb = min(C::NKB, a.S - kb0);
+        if (!mbar_wait_or_abort(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * nkb * RB));
+        __syncwarp();
+        if (lane < C::NREC && rok)
+          bulk_g2s(base + C::NS * GD_B_TILE + rslot * C::RAW_STAGE + lane * (C::NKB * RB),
+                   rec0 + (long long)kb0 * RB, (uint32_t)(nkb * RB), &tl.raw_full[rslot]);
+        if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+      }
+      if (*abort_flag) break;
+    }
+  } else if (warp >= GD_CONV0) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - GD_CONV0 * 32;
+    const int cw = ct >> 5;   // converter warp; TMEM lane quarter = warp % 4 = cw % 4
+    const int q = cw & 3;
+    const int t = MODE == 0 ? (cw >> 2) & 1 : 0;                    // A tile
+    const int j0 = MODE == 0 ? 2 * (cw >> 3) : (cw >> 2);           // first 16-element step
+    const int r = 32 * q + lane;                                    // weight row of the tile
+    const int ri = t * 8 + (r >> 4);                                // record of the stage
+    const int g = r & 7, h = (r >> 3) & 1;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16) + C::A_COL0 + t * 32 + 8 * j0;
+    int slot = 0, rslot = 0;
+    uint32_t phase = 0, rphase = 0;
+    // token rows: threads ct < 32 * 8 copy 16-byte chunk (ct & 7) of row ct >> 3, LA
+    // stages ahead of the conversion so that the copies' latency hides behind the decode.
+    // Every call commits one cp.async group (empty past the last stage), so that waiting
+    // for all but the newest LA groups always means "this stage's rows have landed".
+    const int brow = ct >> 3, ch = ct & 7;
+    int bi = blockIdx.x, bkb = 0, bslot = 0;
+    uint32_t bphase = 0;
+    const uint16_t* rowp = nullptr;
+    auto load_rows = [&](int item) {
+      const GmItem it = gm_item<MODE>(item, a, tl.citem);
+      rowp = nullptr;
+      if (brow < it.n) {
+        const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + brow] / a.k : (it.r0 + brow);
+        rowp = a.act + ar * a.act_ld + ch * 8;
+      }
+    };
+    auto issue_rows = [&]() {  // copies of stage (bi, bkb)
+      if (bi >= nitems || !mbar_wait_or_abort(&tl.empty[bslot], bphase ^ 1u, abort_flag, a.status)) {
+        cp_async_commit();
+        return;
+      }
+      if (rowp) {
+        const bool kok = bkb * 64 + ch * 8 < a.K;  // beyond K: zeros
+        cp_async16(base_addr + bslot * GD_B_TILE + (brow >> 3) * 1024 + (brow & 7) * 128 +
+                       ((ch ^ (brow & 7)) * 16),
+                   kok ? rowp + bkb * 64 : rowp, kok ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (++bslot == C::NS) { bslot = 0; bphase ^= 1u; }
+      if (++bkb == a.S) {
+        bkb = 0;
+        bi += G;
+        if (bi < nitems) load_rows(bi);
+      }
+    };
+    if (MODE == 1) pdl_wait();  // h comes from the gate/up kernel
+    if (bi < nitems) load_rows(bi);
+    for (int s = 0; s < C::LA; ++s) issue_rows();
+    for (int i = blockIdx.x; i < nitems; i += G) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      bool rok;
+      gm_record_row<MODE>(it, ri, a, rok);
+      for (int kb = 0; kb < a.S; ++kb) {
+        const int jkb = kb % C::NKB;  // k-block within the raw super-stage
+        const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
+        issue_rows();
+        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
+        if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after_sync();
+        if (rok) {
+          convert_row<QT, C::NSTEP>(rawring + rslot * C::RAW_STAGE + (ri * C::NKB + jkb) * RB,
+                                    tlane + slot * C::A_STAGE_COLS, g, h, j0);
+          tmem_wait_st();
+        }
+        cp_async_wait<C::LA>();  // this stage's rows have landed
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (last_of_super) mbar_arrive(&tl.raw_empty[rslot]);
+          mbar_arrive(&tl.a_full[slot]);
+        }
+        if (last_of_super && ++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+        if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+      }
+      if (*abort_flag) break;
+    }
+    cp_async_wait<0>();
+  } else if (warp == GD_MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      int slot = 0, buf = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < nitems && ok; i += G) {
+        const GmItem it = gm_item<MODE>(i, a, tl.citem);
+        const int N = max(16, (it.n + 15) & ~15);
+        const uint32_t idesc = idesc_bf16_f32(GD_ROWS, N);
+        if (!mbar_wait_or_abort(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem + buf * C::ACC_COLS;
+        for (int kb = 0; kb < a.S; ++kb) {
+          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t bs = base_addr + slot * GD_B_TILE;
+          const uint32_t as = tmem + C::A_COL0 + slot * C::A_STAGE_COLS;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc_kmajor_sw128(bs + 32 * kk);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+#pragma unroll
+            for (int tt = 0; tt < C::NT; ++tt)
+              mma_bf16_tmem_a(d0 + tt * GD_TOK, as + tt * 32 + 8 * kk, bd, idesc, acc);
+          }
+          mma_commit(&tl.empty[slot]);
+          if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&tl.acc_full[buf]);
+        if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
+      }
+      // every MMA issued above has finished once this arrives
+      mma_commit(&tl.drain);
+      mbar_wait_or_abort(&tl.drain, 0, abort_flag, a.status, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp < GD_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue (warps 0..3)
+    const int q = warp;  // TMEM lanes [32q, 32q + 32) = features 32q.. of the tile
+    // lanes l and l ^ 1 hold adjacent features: they swap values to store bf16 pairs
+    const int odd = lane & 1;
+    const uint32_t stg = staging + q * GD_STG;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int i = blockIdx.x; i < nitems; i += G) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      if (!mbar_wait_or_abort(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
+      tc_fence_after_sync();
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::ACC_COLS;
+      // Each 32 x 16 block (this warp's 32 features x 16 tokens) goes through the warp's
+      // staging tile [token][feature] so that the global stores are 16-byte vectors.
+      const int fw = it.f0 + 32 * q;  // first feature of this warp
+      const bool ok = fw < a.nrows;
+      uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
+      for (int c0 = 0; c0 < it.n; c0 += GD_ECOL) {
+        float v[GD_ECOL];
+        if (MODE == 0) {
+          uint32_t gv[GD_ECOL], uv[GD_ECOL];
+          tmem_ld16(lane_base + c0, gv);
+          tmem_ld16(lane_base + GD_TOK + c0, uv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < GD_ECOL; ++j) {
+            const float gg = __uint_as_float(gv[j]);
+            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
+          }
+        } else {
+          uint32_t yv[GD_ECOL];
+          tmem_ld16(lane_base + c0, yv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < GD_ECOL; ++j) v[j] = __uint_as_float(yv[j]);
+        }
+#pragma unroll
+        for (int p = 0; p < GD_ECOL / 2; ++p) {
+          const float send = odd ? v[2 * p] : v[2 * p + 1];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          const float lo = odd ? recv : v[2 * p];
+          const float hi = odd ? v[2 * p + 1] : recv;
+          const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (lane & ~1) * 2), "r"(w)
+                       : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r4 = 0; r4 < GD_ECOL / 8; ++r4) {
+          const int row = 8 * r4 + (lane >> 2);
+          uint4 d;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+                       : "r"(stg + row * 64 + (lane & 3) * 16)
+                       : "memory");
+          if (ok && c0 + row < it.n)
+            *reinterpret_cast<uint4*>(obase + (long long)(c0 + row) * a.out_ld) = d;
+        }
+        __syncwarp();
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tl.acc_empty[buf]);
+      if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == GD_MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, GD_TMEM_COLS);
+  }
+}
+
+template <int QT, int MODE, class Tab>
+static cudaError_t gd_launch(const GemmArgs& a, const Tab& tab, cudaStream_t st) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorUnknown;
+  constexpr size_t smem = gd_smem_bytes<MODE>();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  cudaError_t err = set_smem_limit<gemm_decode_kernel<QT, MODE, Tab>>(smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(di->sm_count);
+  cfg.blockDim = dim3(GD_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<QT, MODE, Tab>, a, tab);
+}
+
+template <int QT, class Tab>
+static cudaError_t gd_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t st) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorUnknown;
+  GemmArgs a{};
+  a.offsets = pb.offsets;
+  a.sorted_pair = pb.sorted_pair;
+  a.k = pb.k;
+  a.E = pb.E;
+  a.status = di->status;
+  a.act = pb.x;
+  a.act_ld = pb.H;
+  a.K = pb.H;
+  a.out = pb.h_act;
+  a.out_ld = pb.I;
+  a.wbase = pb.w13;
+  a.wstride = (long long)pb.w13_bytes;
+  a.table_off = 0;
+  a.S = slabs_of(pb.H);
+  a.nrows = pb.I;
+  a.up_row0 = pb.I;
+  a.ft_per_expert = (pb.I + GD_ROWS - 1) / GD_ROWS;
+  GemmArgs d = a;
+  d.sorted_pair = nullptr;
+  d.act = pb.h_act;
+  d.act_ld = pb.I;
+  d.K = pb.I;
+  d.out = pb.y_perm;
+  d.out_ld = pb.H;
+  d.wbase = pb.w2;
+  d.wstride = (long long)tiles_bytes_per_expert(pb.qtype, pb.H, pb.I);
+  d.table_off = (long long)pb.w13_bytes;
+  d.S = slabs_of(pb.I);
+  d.nrows = pb.H;
+  d.up_row0 = 0;
+  d.ft_per_expert = (pb.H + GD_ROWS - 1) / GD_ROWS;
+  cudaError_t err = gd_launch<QT, 0>(a, tab, st);
+  if (err != cudaSuccess) return err;
+  return gd_launch<QT, 1>(d, tab, st);
+}
+
+}  // namespace dec
+
+cudaError_t launch_ffn_gemm_decode(const FfnProblem& pb, cudaStream_t st) {
+  if (pb.E > dec::GD_MAX_E) return cudaErrorNotSupported;
+  if (pb.table) {
+    dec::GmWithTable t;
+    t.t = *pb.table;
+    return pb.qtype == FTMOE_Q4_0 ? dec::gd_launch_qt<FTMOE_Q4_0>(pb, t, st)
+                                  : dec::gd_launch_qt<FTMOE_MXFP4>(pb, t, st);
+  }
+  dec::GmNoTable t;
+  return pb.qtype == FTMOE_Q4_0 ? dec::gd_launch_qt<FTMOE_Q4_0>(pb, t, st)
+                                : dec::gd_launch_qt<FTMOE_MXFP4>(pb, t, st);
+}
+
+}  // namespace ftmoe

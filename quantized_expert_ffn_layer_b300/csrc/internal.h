@@ -77,6 +77,9 @@ size_t ffn_gemv_zero_bytes(int T, int k, int E, int H, int I);
 // Grouped GEMM on tcgen05; returns cudaErrorNotSupported when the shape is outside
 // what the kernel handles (callers then use the GEMV path).
 cudaError_t launch_ffn_gemm(const FfnProblem& pb, void* ws, size_t ws_bytes, cudaStream_t st);
+// Grouped GEMM on tcgen05 with 32-token tiles and the decoded weights in tensor memory,
+// for few rows per expert (decode); cudaErrorNotSupported outside its shapes.
+cudaError_t launch_ffn_gemm_decode(const FfnProblem& pb, cudaStream_t st);
 size_t ffn_gemm_ws_bytes(int T, int k, int E, int H, int I);
 
 }  // namespace ftmoe

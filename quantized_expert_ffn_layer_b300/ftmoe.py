@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "NO_S
                 5: "TIMEOUT", 6: "DEVICE_CHECK", 7: "WORKSPACE"}
 Q4_0, MXFP4 = 1, 2
 QTYPES = {"q4_0": Q4_0, "mxfp4": MXFP4}
-PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_GEMM, PATH_GEMM_DECODE = 0, 1, 2, 3
 LRU_PER_LAYER, LRU_GLOBAL = 0, 1
 
 

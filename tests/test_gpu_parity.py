@@ -230,20 +230,33 @@ def test_ragged_shapes_and_shared_expert(env):
     assert rel_l2(out, r["out"]) <= LAYER_TOL
 
 
-def test_gemv_batch_invariance(env):
-    """A token's output does not depend on the other tokens of the batch (bit-exact)."""
+@pytest.mark.parametrize("path", [1, 3])
+def test_decode_batch_invariance(env, path):
+    """A token's output does not depend on the other tokens of the batch (bit-exact),
+    for the mma.sync grouped GEMV (1) and the tensor-memory tcgen05 decode GEMM (3)."""
     c = dict(CONFIGS["decode"])
     c.update(T=64)
     L = make_layer(**c)
     F, torch, dev = env
-    m, out64, _, _ = _layer_gpu(env, L, path=1)
+    m, out64, _, _ = _layer_gpu(env, L, path=path)
     for t in (0, 17, 63):
         x1 = bf16_tensor(L.x[t:t + 1], dev)
         lg1 = torch.from_numpy(L.logits[t:t + 1].copy()).to(dev)
-        old = F.ftmoe_set_ffn_path(1)
+        old = F.ftmoe_set_ffn_path(path)
         o1 = m.forward(lg1, x1, L.k)
         F.ftmoe_set_ffn_path(old)
         assert np.array_equal(bf16_to_f64(o1)[0], out64[t])
+
+
+@pytest.mark.parametrize("qtype", ["q4_0", "mxfp4"])
+def test_gemm_decode_path_ragged_shared_and_multi_tile(env, qtype):
+    """Decode GEMM on ragged H / I (partial 128-row tiles, half-filled last block), a shared
+    expert, and experts with more rows than one 32-token tile."""
+    L = make_layer(H=224, I=96, E=5, k=3, T=60, qtype=qtype, seed=13, shared=True, zipf=1.0)
+    _, out, ids, _ = _layer_gpu(env, L, path=3)
+    r = oracle.layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2, L.shared_w13, L.shared_w2)
+    assert np.array_equal(ids, r["ids"])
+    assert rel_l2(out, r["out"]) <= LAYER_TOL
 
 
 @pytest.mark.parametrize("qtype", ["q4_0", "mxfp4"])
@@ -295,7 +308,7 @@ def test_gemm_path_ragged_shapes_and_shared_expert(env):
     assert rel_l2(out, r["out"]) <= LAYER_TOL
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_expert_blob_table_matches_contiguous_weights(env, path):
     """Weights reached through a per-expert pointer table (cache slots) give the same bits."""
     F, torch, dev = env

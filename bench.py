@@ -141,10 +141,12 @@ def run_reference(args, cfg, L, world, rank):
     """--impl reference: the fp64 oracle as it stands, on this host's cores."""
     if rank != 0:
         return
-    sample_T = min(L.T, args.ref_tokens)
+    # each step is a bounded sample of the batch, sized so that the whole run stays
+    # within about two minutes whatever --steps is (calibrated on one token)
+    _, _, t1 = oracle_cpu_run(L, 1)
+    budget = max(0.25, 120.0 / max(1, args.steps))
+    sample_T = int(max(1, min(L.T, args.ref_tokens, budget / max(t1, 1e-6))))
     vals = []
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; keep the step count honest
     t_all = time.perf_counter()
     threads = 1
     for _ in range(args.steps):
@@ -178,6 +180,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the extra prefill-layer measurement of the default run")
+    ap.add_argument("--stream-steps", type=int, default=256,
+                    help="timed decode steps of the 48-layer expert-cache stream (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -253,6 +257,11 @@ def main():
                            "ms_per_step": float(np.mean(r["step_ms"])),
                            "roofline": ffn_roofline(Lp, r["U"], r["ffn_ms"], pk, pk_kind, wl)}
 
+    # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
+    stream_res = None
+    if args.stream_steps > 0 and args.config == "decode":
+        stream_res = measure_stream(L, dev, args.stream_steps, 16, rank)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_T = min(T, args.ref_tokens)
@@ -280,10 +289,122 @@ def main():
             "clocks": clk.summary(),
             "decode_sweep": sweep or None,
             "prefill": prefill,
+            "stream": stream_res,
         }
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def host_mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def measure_stream(L, dev, steps, warmup, rank):
+    """Batch-1 decode through a stack of layers whose expert weights live in a pinned-host
+    bank and are streamed into a per-layer LRU slot pool (25% of the experts).  Per layer:
+    prefetch the next layer's experts on the copy stream, acquire this layer's (the compute
+    stream waits for their copies), run the layer from the slot pointer table, release.
+    Reports tokens/s, the hit rate, the achieved host->device bandwidth against a plain
+    pinned copy, and the same layers with every expert resident (no cache) for the bound."""
+    import torch
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    from synth import stream_trace
+    c = CONFIGS["stream"]
+    E, k, H, I = L.E, L.k, L.H, L.I
+    m = MoELayer(L.qtype, E, H, I, L.w13, L.w2, device=dev)
+    nb = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
+    layers = c["layers"]
+    # the bank is pinned host memory: keep it within half of what the host has free
+    avail = host_mem_available()
+    if avail and layers * E * nb > avail // 2:
+        layers = max(2, int(avail // 2 // (E * nb)))
+    slots = c["slots"]
+    blobs = torch.cat([m.w13.view(E, -1), m.w2.view(E, -1)], dim=1).cpu()
+    assert blobs.shape[1] == nb
+    bank = torch.empty((layers, E, nb), dtype=torch.uint8, pin_memory=True)
+    for l in range(layers):
+        bank[l].copy_(blobs)  # every layer holds the same expert draws; only the bytes' path matters
+    pool = torch.empty(layers * slots * nb, dtype=torch.uint8, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    compute = torch.cuda.current_stream(dev)
+    cache = F.ExpertCache(layers, E, nb, bank, pool, slots, F.LRU_PER_LAYER, copy_stream)
+    total = warmup + steps
+    trace = stream_trace(c["seed"] + rank, total, layers, E, k, c["p_repeat"], c["zipf"])
+    lg = np.full((total, layers, E), -4.0, dtype=np.float32)
+    for j in range(k):  # routing selects exactly the trace's ids, in trace order
+        np.put_along_axis(lg, trace[:, :, j:j + 1].astype(np.int64), 4.0 - 0.25 * j, axis=2)
+    lg_d = torch.from_numpy(lg).to(dev)
+    x = torch.from_numpy(L.x[:1].view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    ws = m.workspace(1, k)
+    wts = F.make_weights(L.qtype, E, H, I)
+    import ctypes as C
+    wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))  # filled by every acquire
+    ids_py = trace.tolist()
+
+    def run_steps(s0, s1):
+        for st in range(s0, s1):
+            cache.prefetch(0, ids_py[st][0])
+            for l in range(layers):
+                if l + 1 < layers:
+                    cache.prefetch(l + 1, ids_py[st][l + 1])
+                cache.acquire(l, ids_py[st][l], compute)
+                F.ftmoe_layer(wts, lg_d[st, l:l + 1], x, 1, k, out, None, None, ws, ws.numel())
+                cache.release(l, compute)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(compute)
+        fn()
+        b.record(compute)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), (time.perf_counter() - t0) * 1e3
+
+    run_steps(0, warmup)
+    s0 = cache.stats()
+    ms, wall_ms = timed(lambda: run_steps(warmup, total))
+    s1 = cache.stats()
+    d = {f: s1[f] - s0[f] for f in s1}
+    # the same layers with every expert resident (contiguous weights, no cache calls)
+    def resident():
+        for st in range(warmup, total):
+            for l in range(layers):
+                F.ftmoe_layer(m.weights, lg_d[st, l:l + 1], x, 1, k, out, None, None, ws, ws.numel())
+    res_ms, res_wall = timed(resident)
+    # plain pinned host -> device copy bandwidth (the PCIe ceiling for the misses)
+    src = bank.view(-1)[: 1 << 30]
+    dst = torch.empty(src.numel(), dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    cp_ms, _ = timed(lambda: [dst.copy_(src, non_blocking=True) for _ in range(4)])
+    pcie_gbs = 4 * src.numel() / (cp_ms / 1e3) / 1e9
+    h2d_gbs = d["h2d_bytes"] / (ms / 1e3) / 1e9
+    bound_ms = max(res_ms, d["h2d_bytes"] / (pcie_gbs * 1e9) * 1e3)
+    cache.close()
+    out_d = {"workload": f"batch-1 decode, {layers} layers H{H} I{I} E{E} top-{k} {L.qtype}, "
+                         f"{slots} slots per layer (LRU), trace p_repeat {c['p_repeat']} Zipf {c['zipf']}",
+             "layers": layers, "steps": steps, "warmup_steps": warmup,
+             "tokens_per_s": steps / (ms / 1e3), "ms_per_token": ms / steps,
+             "host_wall_ms_per_token": wall_ms / steps,
+             "hit_rate": d["hits"] / max(1, d["lookups"]),
+             "misses_per_token": d["misses"] / steps, "prefetch_copies_per_token": d["prefetch_copies"] / steps,
+             "h2d_bytes_per_token": d["h2d_bytes"] / steps, "h2d_gbs": h2d_gbs,
+             "pinned_copy_gbs": pcie_gbs, "h2d_frac": h2d_gbs / pcie_gbs,
+             "resident_ms_per_token": res_ms / steps,
+             "bound_ms_per_token": bound_ms / steps, "frac_of_bound": bound_ms / ms}
+    del bank, pool, dst
+    torch.cuda.empty_cache()
+    return out_d
 
 
 def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload):

@@ -225,6 +225,15 @@ ftmoe_status ftmoe_layer(const ftmoe_weights* wts, const float* logits, const ui
  * until `stream` is idle.  *code_out = 0 if nothing was recorded. */
 ftmoe_status ftmoe_device_status(int* code_out, ftmoe_stream_t stream);
 
+/* Self-check of the bounded waits (no counterpart on the pages).  Launches one
+ * CTA that waits on an mbarrier nothing arrives on, with the bounded wait the
+ * pipelined kernels use and a limit of limit_ns nanoseconds of GPU wall time
+ * (1e3 <= limit_ns <= 1e9, else FTMOE_ERR_INVALID_ARG).  The wait gives up, ORs
+ * 2 (wait ran out) into the status word that ftmoe_device_status reads, writes 0
+ * to *waited_ok (device int, nullable) and the kernel returns normally: the
+ * context stays usable.  Asynchronous on `stream`. */
+ftmoe_status ftmoe_check_wait_timeout(long long limit_ns, int* waited_ok, ftmoe_stream_t stream);
+
 /* ------------------------------------------------------------------ expert cache
  * [P5] §五 / [P3] 机制四: cold experts live in a pinned host bank, hot ones in a
  * device slot pool managed by LRU; [P3] 机制一: the next layer's experts are

@@ -3,25 +3,31 @@
 // Q4_0 / MXFP4 banks, with the block decode of §六 done by the SM into tensor memory.
 //
 // Decode reads every selected expert's weights once for a handful of tokens, so the
-// layer is bound by streaming the 4-bit weights from HBM.  One persistent CTA per SM
-// works through items (expert, 128 weight rows, up to 32 of the expert's token rows):
-// for gate/up the gate and the up rows of 128 features (two A tiles), for down one
-// 128-row tile.  Per 64-element reduction block ("stage"):
+// layer is bound by streaming the 4-bit weights from HBM, and what limits a kernel is
+// the number of instructions it spends per weight.  One persistent CTA per SM works
+// through items (expert, 128 weight rows, up to 16 of the expert's token rows): for
+// gate/up the gate and the up rows of 128 features (two A tiles), for down one 128-row
+// tile.  Per 64-element reduction slab ("stage"):
 //   * a raw-weight warp keeps a deep ring of shared-memory slots filled with the
-//     stage's 4-bit weight records (1-D bulk copies) and warms L2 with the next item;
-//   * 16 converter warps decode the records into exact bf16 (round-to-nearest-even of
-//     the decoded value); each thread owns one weight row (its tensor-memory lane) and
-//     writes its columns of the A tile with tcgen05.st; they also gather the item's
-//     token rows (x for gate/up through the permutation, h for down) with cp.async
-//     into the 128-byte-swizzled K-major B tile;
-//   * one thread issues tcgen05.mma kind::f16 with A from tensor memory and B from
-//     shared memory (M = 128, N = the token count rounded up to 16, K = 16);
-//   * 4 epilogue warps read the accumulators with tcgen05.ld (two buffers, so the
-//     epilogue of one item overlaps the MMAs of the next) and store h = silu(g) * u or
-//     y as bf16.
-// The multiply-accumulate order over the reduction dimension is fixed and each output
-// depends only on its own weight row and token row, so a token's result does not
-// depend on the other tokens of the batch.
+//     stage's 4-bit weight records (one 1-D bulk copy per record row group and four
+//     stages) and warms L2 with the CTA's next item;
+//   * 8 converter warps turn each 16-row record into bf16 codes: q - 8 for Q4_0 (an
+//     integer in [-8, 7]) or the E2M1 value for MXFP4, both exact and unscaled.  Lane
+//     4g + c of a record holds elements 4c..4c+3 of every 16-element step for rows g
+//     and g + 8, which is exactly the thread layout of the 16x256b tensor-memory store,
+//     so every lane decodes its own 16 bytes and stores them without any exchange;
+//     they also gather the item's token rows (x through the permutation for gate/up, h
+//     for down) with cp.async into the 128-byte-swizzled K-major B tile;
+//   * one thread issues tcgen05.mma kind::f16 (A from tensor memory, B from shared
+//     memory, M = 128, N = 16, K = 16) into one fresh partial-sum accumulator per
+//     32-element quantization block;
+//   * 4 epilogue warps read the partial sums with tcgen05.ld and add block scale x
+//     partial sum into fp32 registers (one weight row per thread), then store
+//     h = silu(g) * u or y as bf16.
+// So the only roundings are the fp32 sums, the bf16 h between the projections and the
+// bf16 output, as in the grouped GEMV.  The order of every sum is fixed and each output
+// depends only on its own weight row and token row, so a token's result does not depend
+// on the other tokens of the batch.
 #include <mutex>
 
 #include "common.cuh"
@@ -32,53 +38,47 @@
 namespace ftmoe {
 namespace dec {
 
-constexpr int GD_TOK = 32;          // token rows per item (largest MMA N)
+constexpr int GD_TOK = 16;          // token rows per item (MMA N)
 constexpr int GD_ROWS = 128;        // weight rows per tile (MMA M, TMEM lanes)
 constexpr int GD_EPI_WARPS = 4;     // warps 0..3 (one per TMEM lane quarter)
 constexpr int GD_MMA_WARP = 4;      // TMEM owner; lane 0 issues the MMAs
 constexpr int GD_RAW_WARP = 5;      // bulk copies of the raw weight records; warps 6, 7 idle
 constexpr int GD_CONV0 = 8;         // first converter warp (a multiple of 4)
-constexpr int GD_CONV_WARPS = 16;
-constexpr int GD_CONV_THREADS = GD_CONV_WARPS * 32;
-constexpr int GD_THREADS = (GD_CONV0 + GD_CONV_WARPS) * 32;  // 768
+constexpr int GD_CONV_WARPS = 8;
+constexpr int GD_THREADS = (GD_CONV0 + GD_CONV_WARPS) * 32;  // 512
 constexpr uint32_t GD_TMEM_COLS = 512;
-constexpr int GD_B_TILE = GD_TOK * 128;   // 4 KB of bf16 (32 token rows x 64)
-constexpr int GD_ECOL = 16;               // accumulator columns (tokens) per epilogue step
-constexpr int GD_STG = GD_ECOL * 64;      // epilogue staging per warp: 16 rows x 32 bf16
+constexpr int GD_B_TILE = GD_TOK * 128;   // 2 KB of bf16 (16 token rows x 64)
+constexpr int GD_STG = GD_TOK * 64;       // epilogue staging per warp: 16 rows x 32 bf16
 constexpr int GD_MAX_E = 1024;
-constexpr int GD_MAX_NR = 16;
+constexpr int GD_MAX_NR = 8;
 constexpr int GD_MAX_NS = 8;
 
-// Per-projection layout.  Tensor-memory columns: two accumulator buffers of NT x 32
-// columns, then NS stages of A tiles (NT x 32 columns: 64 bf16 per lane).  The raw
-// weight ring (shared memory) holds super-stages of NKB consecutive k-blocks, filled
-// with one bulk copy per record row group (records of a row group are contiguous along
-// the reduction dimension), so that enough HBM reads are in flight with few copy ops.
+// Per-projection layout.  Tensor-memory columns: NPS partial-sum stages (per A tile
+// and quantization block, GD_TOK fp32 columns), then NS stages of A tiles (NT x 32
+// columns: 64 bf16 per lane).  The raw weight ring (shared memory) holds super-stages
+// of NKB consecutive slabs, filled with one bulk copy per record row group (the records
+// of a row group are contiguous along the reduction dimension).
 template <int MODE>
 struct GdCfg {
   static constexpr int NT = MODE == 0 ? 2 : 1;            // A tiles (MMAs per k-step)
-  static constexpr int NACC = 2;                          // accumulator buffers
-  static constexpr int NS = MODE == 0 ? 6 : 8;            // A / B stages
-  static constexpr int LA = NS - 3;                       // token-row copy stages in flight
-  static constexpr int NKB = 4;                           // k-blocks per raw super-stage
-  static constexpr int NR = MODE == 0 ? 3 : 4;            // raw weight super-stages
+  static constexpr int NS = MODE == 0 ? 4 : 8;            // A / B stages
+  static constexpr int NPS = MODE == 0 ? 4 : 8;           // partial-sum stages
+  static constexpr int LA = NS / 2;                       // token-row copy stages in flight
+  static constexpr int NKB = 4;                           // slabs per raw super-stage
+  static constexpr int NR = MODE == 0 ? 4 : 6;            // raw weight super-stages
   static constexpr int NREC = 8 * NT;                     // weight records per stage
-  static constexpr int RAW_STAGE = NREC * NKB * 576;      // [record][k-block][576]
-  static constexpr int ACC_COLS = NT * GD_TOK;            // columns of one accumulator buffer
-  static constexpr int A_COL0 = NACC * ACC_COLS;          // first A-stage column
+  static constexpr int RAW_STAGE = NREC * NKB * 576;      // [record][slab][576]
+  static constexpr int PS_STAGE_COLS = NT * 2 * GD_TOK;   // [tile][block][token]
+  static constexpr int A_COL0 = NPS * PS_STAGE_COLS;
   static constexpr int A_STAGE_COLS = NT * 32;
   static_assert(A_COL0 + NS * A_STAGE_COLS <= (int)GD_TMEM_COLS, "tensor memory columns");
-  static_assert(NS <= GD_MAX_NS && NR <= GD_MAX_NR && LA >= 1, "ring sizes");
-  // converter threads: one weight row each (its TMEM lane), covering 64 / CPR
-  // reduction elements of the stage (CPR = converter threads per row)
-  static constexpr int CPR = GD_CONV_THREADS / (NT * GD_ROWS);
-  static constexpr int NSTEP = 4 / CPR;                   // 16-element steps per thread
+  static_assert(NS <= GD_MAX_NS && NPS <= GD_MAX_NS && NR <= GD_MAX_NR && LA >= 1, "ring sizes");
 };
 
 struct GdTail {
   uint64_t raw_full[GD_MAX_NR], raw_empty[GD_MAX_NR];
   uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS];
-  uint64_t acc_full[2], acc_empty[2], drain;
+  uint64_t ps_full[GD_MAX_NS], ps_empty[GD_MAX_NS], drain;
   uint32_t tmem_base;
   int abort_flag;
   int citem[GD_MAX_E + 1];  // exclusive prefix of items per expert
@@ -88,6 +88,7 @@ constexpr size_t gd_smem_bytes() {
   return 1024 + (size_t)GdCfg<MODE>::NS * GD_B_TILE + (size_t)GdCfg<MODE>::NR * GdCfg<MODE>::RAW_STAGE +
          (size_t)GD_EPI_WARPS * GD_STG + sizeof(GdTail);
 }
+
 
 struct GemmArgs {
   const int32_t* offsets;
@@ -154,23 +155,6 @@ __device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const Gem
 }
 
 // ---------------------------------------------------------------- weight decode
-// Block scale of one row as (hi, lo) bf16x2 pairs with hi + lo == the scale exactly
-// (Q4_0 fp16 d), or (2^(e-127), 0) for an MXFP4 E8M0 byte.
-template <int QT>
-__device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
-  if (QT == FTMOE_Q4_0) {
-    const float d = half_bits_to_f32(bits);
-    const uint32_t hi = f32_to_bf16_bits(d);
-    const uint32_t lo = f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
-    hi2 = hi | (hi << 16);
-    lo2 = lo | (lo << 16);
-  } else {
-    const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
-    hi2 = b | (b << 16);
-    lo2 = 0;
-  }
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -188,36 +172,40 @@ __device__ __forceinline__ uint2 lds64(uint32_t saddr) {
   return v;
 }
 
-// Two bf16x2 pairs (elements 0,1 and 2,3 of a 4-element group) from a nibble word E whose
-// bytes hold the group's codes in the order (e0, e2, e1, e3), each in the low nibble.
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
+// bf16x2 codes of elements (0, 1) and (2, 3) of a 4-element group from a word whose
+// bytes hold the group's 4-bit codes in the order (e0, e2, e1, e3), one per low nibble:
+// q - 8 for Q4_0, the E2M1 value for MXFP4.  Both are exact in bf16.
 template <int QT>
-__device__ __forceinline__ void decode_group(uint32_t E, uint32_t s_hi, uint32_t s_lo, uint32_t& o0,
-                                             uint32_t& o1) {
+__device__ __forceinline__ void decode_plain(uint32_t E, uint32_t& o0, uint32_t& o1) {
   if (QT == FTMOE_Q4_0) {
     const uint32_t K = 0x43434343u;  // high byte of bf16 128: (128 + q) per element
-    const uint32_t t[2] = {prmt(E, K, 0x4240u), prmt(E, K, 0x4341u)};
     const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-    uint32_t r[2];
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      // RNE((q - 8) * d) with d = hi + lo split exactly
-      const __nv_bfloat162 u = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t[p]), off);
-      const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
-      const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
-      r[p] = *reinterpret_cast<const uint32_t*>(&w);
-    }
-    o0 = r[0];
-    o1 = r[1];
+    uint32_t t0 = prmt(E, K, 0x4240u), t1 = prmt(E, K, 0x4341u);
+    const __nv_bfloat162 u0 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t0), off);
+    const __nv_bfloat162 u1 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t1), off);
+    o0 = *reinterpret_cast<const uint32_t*>(&u0);
+    o1 = *reinterpret_cast<const uint32_t*>(&u1);
   } else {
-    const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
     const uint32_t TWO126 = 0x7E807E80u;
+    const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
     uint32_t r[2];
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      uint32_t t = ((v[p] & 0x00070007u) << 6) | ((v[p] & 0x00080008u) << 12);  // E2M1 * 2^-126
-      __nv_bfloat162 w = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&t),
-                                 *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
-      w = __hmul2(w, *reinterpret_cast<const __nv_bfloat162*>(&s_hi));
+      // ((c & 7) << 6) | ((c & 8) << 12) read as bf16 is E2M1(c) * 2^-126 (the E2M1
+      // subnormal lands on a bf16 subnormal); one bf16 multiply by 2^126 makes it exact
+      uint32_t t = ((v[p] & 0x00070007u) << 6) | ((v[p] & 0x00080008u) << 12);
+      const __nv_bfloat162 w = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
       r[p] = *reinterpret_cast<const uint32_t*>(&w);
     }
     o0 = r[0];
@@ -225,55 +213,35 @@ __device__ __forceinline__ void decode_group(uint32_t E, uint32_t s_hi, uint32_t
   }
 }
 
-// One converter thread decodes NSTEP 16-element steps (from J0) of one weight row and
-// writes them to its tensor-memory lane.  The row is row g + 8 h of a record in shared
-// memory; record lane 4g + c holds, in word j, elements 16j + 4c + (0..3) of rows g and
-// g + 8 (row g in nibble slots 0,4,2,6, row g + 8 in slots 1,5,3,7).  The four segment
-// loads are issued in an order rotated by (g >> 1) so that the 8 rows g of a record read
-// 8 different bank groups, then put back in segment order.
-template <int QT, int NSTEP>
-__device__ __forceinline__ void convert_row(uint32_t rec, uint32_t taddr, int g, int h, int j0) {
-  const int rot = (g >> 1) & 3;
-  uint32_t w[4][NSTEP];
+// One converter warp decodes a 16-row x 64-element record into its 16 tensor-memory
+// lanes (the A tile rows of the record) at `taddr`.  Lane L = 4g + c reads its own 16
+// bytes: word j holds elements 16j + 4c + (0..3) of row g in the low nibbles (bytes in
+// the order e0, e2, e1, e3) and of row g + 8 in the high nibbles.  In the 16x256b store
+// shape register 4j + m of lane 4g + c goes to row g + 8 (m >> 1), column
+// 8j + 2c + (m & 1) (two bf16 per 32-bit column), which is where those elements belong.
+template <int QT>
+__device__ __forceinline__ void convert_record(uint32_t rec, uint32_t taddr, int lane) {
+  const uint4 q = lds128(rec + lane * 16);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t out[16];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t addr = rec + (4 * g + ((i + rot) & 3)) * 16 + 4 * j0;
-    if constexpr (NSTEP == 2) {
-      const uint2 v = lds64(addr);
-      w[i][0] = v.x;
-      w[i][NSTEP - 1] = v.y;
-    } else {
-      w[i][0] = lds32(addr);
-    }
+  for (int j = 0; j < 4; ++j) {
+    decode_plain<QT>(w[j] & 0x0F0F0F0Fu, out[4 * j + 0], out[4 * j + 1]);
+    decode_plain<QT>((w[j] >> 4) & 0x0F0F0F0Fu, out[4 * j + 2], out[4 * j + 3]);
   }
-  // v[c] = w[(c - rot) & 3]
-  uint32_t v[4][NSTEP];
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int s = 0; s < NSTEP; ++s) {
-      const uint32_t x0 = w[c][s], x1 = w[(c + 3) & 3][s], x2 = w[(c + 2) & 3][s], x3 = w[(c + 1) & 3][s];
-      v[c][s] = rot == 0 ? x0 : rot == 1 ? x1 : rot == 2 ? x2 : x3;
-    }
-  // block scale of this row
-  uint32_t sh, sl;
-  {
-    const int idx = (g * 2 + (j0 >> 1)) * 2 + h;
-    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
-    const uint32_t wd = lds32(rec + REC_CODE_BYTES + (byte & ~3));
-    const uint32_t bits = QT == FTMOE_Q4_0 ? (wd >> (8 * (byte & 3))) & 0xFFFFu
-                                           : (wd >> (8 * (byte & 3))) & 0xFFu;
-    row_scale<QT>(bits, sh, sl);
+  tmem_st_16x256b_x4(taddr, out);
+}
+
+// Block scale of weight row g + 8 h of a record for quantization block b, as fp32.
+template <int QT>
+__device__ __forceinline__ float record_scale(uint32_t rec, int g, int h, int b) {
+  if (QT == FTMOE_Q4_0) {
+    const uint32_t wd = lds32(rec + REC_CODE_BYTES + g * 8 + b * 4);
+    return half_bits_to_f32(h ? (wd >> 16) : (wd & 0xFFFFu));
+  } else {
+    const uint32_t wd = lds32(rec + REC_CODE_BYTES + g * 4);
+    return e8m0_to_f32((wd >> (8 * (2 * b + h))) & 0xFFu);
   }
-  uint32_t out[8 * NSTEP];
-  const int hs = 4 * h;
-#pragma unroll
-  for (int s = 0; s < NSTEP; ++s)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      decode_group<QT>((v[c][s] >> hs) & 0x0F0F0F0Fu, sh, sl, out[8 * s + 2 * c], out[8 * s + 2 * c + 1]);
-  if constexpr (NSTEP == 2) tmem_st16(taddr, out);
-  else tmem_st8(taddr, out);
 }
 
 // 16-byte global -> shared copy (LDGSTS); src_bytes = 0 writes zeros.
@@ -312,15 +280,15 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < C::NR; ++s) {
       mbar_init(&tl.raw_full[s], 1);
-      mbar_init(&tl.raw_empty[s], GD_CONV_WARPS);
+      mbar_init(&tl.raw_empty[s], GD_CONV_WARPS + GD_EPI_WARPS);  // codes and scales read
     }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&tl.a_full[s], GD_CONV_WARPS);
       mbar_init(&tl.empty[s], 1);
     }
-    for (int b = 0; b < C::NACC; ++b) {
-      mbar_init(&tl.acc_full[b], 1);
-      mbar_init(&tl.acc_empty[b], GD_EPI_WARPS * 32);
+    for (int s = 0; s < C::NPS; ++s) {
+      mbar_init(&tl.ps_full[s], 1);
+      mbar_init(&tl.ps_empty[s], GD_EPI_WARPS);
     }
     mbar_init(&tl.drain, 1);
     tl.abort_flag = 0;
@@ -330,7 +298,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     tmem_alloc(&tl.tmem_base, GD_TMEM_COLS);
     tmem_relinquish();
   }
-  // items per expert: ceil(n_e / 32) token tiles x weight-row slices
+  // items per expert: ceil(n_e / GD_TOK) token tiles x weight-row slices
   if (warp == 0) {
     int carry = 0;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
@@ -390,17 +358,12 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   } else if (warp >= GD_CONV0) {
     // ------------------------------------------------------------ converters
     const int ct = tid - GD_CONV0 * 32;
-    const int cw = ct >> 5;   // converter warp; TMEM lane quarter = warp % 4 = cw % 4
-    const int q = cw & 3;
-    const int t = MODE == 0 ? (cw >> 2) & 1 : 0;                    // A tile
-    const int j0 = MODE == 0 ? 2 * (cw >> 3) : (cw >> 2);           // first 16-element step
-    const int r = 32 * q + lane;                                    // weight row of the tile
-    const int ri = t * 8 + (r >> 4);                                // record of the stage
-    const int g = r & 7, h = (r >> 3) & 1;
-    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16) + C::A_COL0 + t * 32 + 8 * j0;
+    const int cw = ct >> 5;          // converter warp; its TMEM lane quarter = cw % 4
+    const int grp = 2 * (cw & 3) + (cw >> 2);  // record row group: TMEM lanes 16 grp ..
+    const uint32_t tlane = tmem + ((uint32_t)(16 * grp) << 16) + C::A_COL0;
     int slot = 0, rslot = 0;
     uint32_t phase = 0, rphase = 0;
-    // token rows: threads ct < 32 * 8 copy 16-byte chunk (ct & 7) of row ct >> 3, LA
+    // token rows: threads ct < GD_TOK * 8 copy 16-byte chunk (ct & 7) of row ct >> 3, LA
     // stages ahead of the conversion so that the copies' latency hides behind the decode.
     // Every call commits one cp.async group (empty past the last stage), so that waiting
     // for all but the newest LA groups always means "this stage's rows have landed".
@@ -441,17 +404,19 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       bool rok;
-      gm_record_row<MODE>(it, ri, a, rok);
+      gm_record_row<MODE>(it, grp, a, rok);  // the same row group in every tile
       for (int kb = 0; kb < a.S; ++kb) {
-        const int jkb = kb % C::NKB;  // k-block within the raw super-stage
+        const int jkb = kb % C::NKB;  // slab within the raw super-stage
         const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
         issue_rows();
         if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
         if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
         if (rok) {
-          convert_row<QT, C::NSTEP>(rawring + rslot * C::RAW_STAGE + (ri * C::NKB + jkb) * RB,
-                                    tlane + slot * C::A_STAGE_COLS, g, h, j0);
+#pragma unroll
+          for (int t = 0; t < C::NT; ++t)
+            convert_record<QT>(rawring + rslot * C::RAW_STAGE + ((t * 8 + grp) * C::NKB + jkb) * RB,
+                               tlane + slot * C::A_STAGE_COLS + t * 32, lane);
           tmem_wait_st();
         }
         cp_async_wait<C::LA>();  // this stage's rows have landed
@@ -471,38 +436,34 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   } else if (warp == GD_MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      int slot = 0, buf = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int slot = 0, ps = 0;
+      uint32_t phase = 0, pphase = 0;
+      const uint32_t idesc = idesc_bf16_f32(GD_ROWS, GD_TOK);
       bool ok = true;
       for (int i = blockIdx.x; i < nitems && ok; i += G) {
-        const GmItem it = gm_item<MODE>(i, a, tl.citem);
-        const int N = max(16, (it.n + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(GD_ROWS, N);
-        if (!mbar_wait_or_abort(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
-        tc_fence_after_sync();
-        const uint32_t d0 = tmem + buf * C::ACC_COLS;
         for (int kb = 0; kb < a.S; ++kb) {
-          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status)) {
+          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status) ||
+              !mbar_wait_or_abort(&tl.ps_empty[ps], pphase ^ 1u, abort_flag, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t bs = base_addr + slot * GD_B_TILE;
           const uint32_t as = tmem + C::A_COL0 + slot * C::A_STAGE_COLS;
+          const uint32_t pd = tmem + ps * C::PS_STAGE_COLS;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {  // k16 step; block kk / 2 starts from zero
             const uint64_t bd = sdesc_kmajor_sw128(bs + 32 * kk);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
 #pragma unroll
-            for (int tt = 0; tt < C::NT; ++tt)
-              mma_bf16_tmem_a(d0 + tt * GD_TOK, as + tt * 32 + 8 * kk, bd, idesc, acc);
+            for (int t = 0; t < C::NT; ++t)
+              mma_bf16_tmem_a(pd + (t * 2 + (kk >> 1)) * GD_TOK, as + t * 32 + 8 * kk, bd, idesc,
+                              (uint32_t)(kk & 1));
           }
           mma_commit(&tl.empty[slot]);
+          mma_commit(&tl.ps_full[ps]);
           if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+          if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
         }
-        if (!ok) break;
-        mma_commit(&tl.acc_full[buf]);
-        if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
       }
       // every MMA issued above has finished once this arrives
       mma_commit(&tl.drain);
@@ -511,68 +472,101 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     __syncwarp();
   } else if (warp < GD_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue (warps 0..3)
-    const int q = warp;  // TMEM lanes [32q, 32q + 32) = features 32q.. of the tile
+    const int q = warp;                 // TMEM lanes [32q, 32q + 32): weight rows of the tile
+    const int r = 32 * q + lane;
+    const int grp = r >> 4, g = r & 7, h = (r >> 3) & 1;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     // lanes l and l ^ 1 hold adjacent features: they swap values to store bf16 pairs
     const int odd = lane & 1;
     const uint32_t stg = staging + q * GD_STG;
-    int buf = 0;
-    uint32_t acc_phase = 0;
+    int ps = 0, rslot = 0;
+    uint32_t pphase = 0, rphase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
-      if (!mbar_wait_or_abort(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
-      tc_fence_after_sync();
-      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::ACC_COLS;
-      // Each 32 x 16 block (this warp's 32 features x 16 tokens) goes through the warp's
-      // staging tile [token][feature] so that the global stores are 16-byte vectors.
-      const int fw = it.f0 + 32 * q;  // first feature of this warp
-      const bool ok = fw < a.nrows;
-      uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
-      for (int c0 = 0; c0 < it.n; c0 += GD_ECOL) {
-        float v[GD_ECOL];
-        if (MODE == 0) {
-          uint32_t gv[GD_ECOL], uv[GD_ECOL];
-          tmem_ld16(lane_base + c0, gv);
-          tmem_ld16(lane_base + GD_TOK + c0, uv);
+      const int nch = (it.n + 3) >> 2;  // 4-token chunks with real tokens
+      float acc[C::NT][GD_TOK];
+#pragma unroll
+      for (int t = 0; t < C::NT; ++t)
+#pragma unroll
+        for (int j = 0; j < GD_TOK; ++j) acc[t][j] = 0.f;
+      bool ok = true;
+      for (int kb = 0; kb < a.S; ++kb) {
+        const int jkb = kb % C::NKB;
+        const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
+        // (the raw slot is already full: the wait only orders its scale bytes before
+        // the reads below)
+        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status) ||
+            !mbar_wait_or_abort(&tl.ps_full[ps], pphase, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool b1 = kb * 64 + 32 < a.K;  // the slab's second block lies inside K
+#pragma unroll
+        for (int t = 0; t < C::NT; ++t) {
+          const uint32_t rec = rawring + rslot * C::RAW_STAGE + ((t * 8 + grp) * C::NKB + jkb) * RB;
+          const float d0 = record_scale<QT>(rec, g, h, 0);
+          const float d1 = b1 ? record_scale<QT>(rec, g, h, 1) : 0.f;
+          uint32_t p0[GD_TOK], p1[GD_TOK];
+          const uint32_t pc = lane_base + ps * C::PS_STAGE_COLS + t * 2 * GD_TOK;
+          tmem_ld16(pc, p0);
+          tmem_ld16(pc + GD_TOK, p1);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < GD_ECOL; ++j) {
-            const float gg = __uint_as_float(gv[j]);
-            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
+          for (int c = 0; c < GD_TOK / 4; ++c) {
+            if (c < nch) {
+#pragma unroll
+              for (int j = 4 * c; j < 4 * c + 4; ++j) {
+                acc[t][j] = fmaf(d0, __uint_as_float(p0[j]), acc[t][j]);
+                if (b1) acc[t][j] = fmaf(d1, __uint_as_float(p1[j]), acc[t][j]);
+              }
+            }
           }
-        } else {
-          uint32_t yv[GD_ECOL];
-          tmem_ld16(lane_base + c0, yv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < GD_ECOL; ++j) v[j] = __uint_as_float(yv[j]);
         }
-#pragma unroll
-        for (int p = 0; p < GD_ECOL / 2; ++p) {
-          const float send = odd ? v[2 * p] : v[2 * p + 1];
-          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-          const float lo = odd ? recv : v[2 * p];
-          const float hi = odd ? v[2 * p + 1] : recv;
-          const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (lane & ~1) * 2), "r"(w)
-                       : "memory");
-        }
+        tc_fence_before_sync();
         __syncwarp();
-#pragma unroll
-        for (int r4 = 0; r4 < GD_ECOL / 8; ++r4) {
-          const int row = 8 * r4 + (lane >> 2);
-          uint4 d;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-                       : "r"(stg + row * 64 + (lane & 3) * 16)
-                       : "memory");
-          if (ok && c0 + row < it.n)
-            *reinterpret_cast<uint4*>(obase + (long long)(c0 + row) * a.out_ld) = d;
+        if (lane == 0) {
+          mbar_arrive(&tl.ps_empty[ps]);
+          if (last_of_super) mbar_arrive(&tl.raw_empty[rslot]);
         }
-        __syncwarp();
+        if (last_of_super && ++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+        if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
       }
-      tc_fence_before_sync();
-      mbar_arrive(&tl.acc_empty[buf]);
-      if (++buf == C::NACC) { buf = 0; acc_phase ^= 1u; }
+      if (!ok) break;
+      // ---- item result: h = silu(gate) * up, or y; row r of the tile for tokens 0..n-1.
+      // The warp's 32 features x 16 tokens go through its staging tile [token][feature]
+      // so that the global stores are 16-byte vectors.
+      float v[GD_TOK];
+#pragma unroll
+      for (int j = 0; j < GD_TOK; ++j) {
+        if (MODE == 0) {
+          const float gg = acc[0][j];
+          v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * acc[C::NT - 1][j];
+        } else {
+          v[j] = acc[0][j];
+        }
+      }
+      const int fw = it.f0 + 32 * q;  // first feature of this warp
+      const bool fok = fw < a.nrows;
+      uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
+#pragma unroll
+      for (int p = 0; p < GD_TOK / 2; ++p) {
+        const float send = odd ? v[2 * p] : v[2 * p + 1];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        const float lo = odd ? recv : v[2 * p];
+        const float hi = odd ? v[2 * p + 1] : recv;
+        const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (lane & ~1) * 2), "r"(w)
+                     : "memory");
+      }
+      __syncwarp();
+#pragma unroll
+      for (int r4 = 0; r4 < GD_TOK / 8; ++r4) {
+        const int row = 8 * r4 + (lane >> 2);
+        const uint4 d = lds128(stg + row * 64 + (lane & 3) * 16);
+        if (fok && row < it.n) *reinterpret_cast<uint4*>(obase + (long long)row * a.out_ld) = d;
+      }
+      __syncwarp();
     }
   }
 

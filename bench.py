@@ -91,7 +91,9 @@ TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "expert_ffn_gemv": ["gemv.cu", "common.cuh", "pipeline.cuh"],
     "expert_ffn_gemm": ["gemm_sm103.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
+    "expert_ffn_gemm_decode": ["gemm_decode.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
 }
+FFN_PATHS = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_decode": 3}
 
 
 def kernel_src_hash(kernel: str) -> str:
@@ -180,6 +182,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the extra prefill-layer measurement of the default run")
+    ap.add_argument("--ffn-path", default="auto", choices=list(FFN_PATHS),
+                    help="expert-FFN kernel (auto: GEMM at >= 32 rows per expert, else GEMV)")
     ap.add_argument("--stream-steps", type=int, default=256,
                     help="timed decode steps of the 48-layer expert-cache stream (0: skip)")
     args = ap.parse_args()
@@ -214,7 +218,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    from quantized_expert_ffn_layer_b300 import ftmoe as F  # noqa: F401  (fails loudly without libftmoe)
+    from quantized_expert_ffn_layer_b300 import ftmoe as F  # fails loudly without libftmoe
+    F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -227,7 +232,7 @@ def main():
     P = T * k
     tokens_all = T * args.steps * world
     value = tokens_all / (head["max_ms"] / 1e3)
-    roofline = ffn_roofline(L, U, head["ffn_ms"], pk, pk_kind, cfg["workload"])
+    roofline = ffn_roofline(L, U, head["ffn_ms"], pk, pk_kind, cfg["workload"], args.ffn_path)
     e2e_val = tokens_all / (head["e2e_max_ms"] / 1e3)
 
     # ---- decode sweep over the other batch sizes (informative)
@@ -241,12 +246,14 @@ def main():
             r = measure_layer(Ls, dev, max(20, args.steps // 2), 3, flush, stream, None, e2e=False)
             sweep[str(Ts)] = {"tokens_per_s": Ts / (np.mean(r["step_ms"]) / 1e3),
                               "ms": float(np.mean(r["step_ms"])),
-                              "ffn_hbm_frac": ffn_roofline(Ls, r["U"], r["ffn_ms"], pk, pk_kind, "")["frac"]}
+                              "ffn_hbm_frac": ffn_roofline(Ls, r["U"], r["ffn_ms"], pk, pk_kind, "",
+                                                           args.ffn_path)["frac"]}
 
     # ---- the compute-bound prefill layer (same shape, 4096 tokens), Q4_0 and MXFP4
     prefill = None
     if not args.no_prefill and args.config == "decode":
         prefill = {}
+        F.ftmoe_set_ffn_path(FFN_PATHS["auto"])  # the prefill line always takes the library's choice
         for qt in CONFIGS["prefill"]["qtypes"]:
             cp = dict(CONFIGS["prefill"])
             cp["qtype"] = qt
@@ -256,6 +263,7 @@ def main():
             prefill[qt] = {"workload": wl, "tokens_per_s": Lp.T / (np.mean(r["step_ms"]) / 1e3),
                            "ms_per_step": float(np.mean(r["step_ms"])),
                            "roofline": ffn_roofline(Lp, r["U"], r["ffn_ms"], pk, pk_kind, wl)}
+        F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
 
     # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
     stream_res = None
@@ -278,7 +286,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
             "config": {"workload": cfg["workload"], "H": H, "I": I, "E": E, "k": k, "T": T,
-                       "qtype": L.qtype, "parallelism": f"replicas{world}",
+                       "qtype": L.qtype, "parallelism": f"replicas{world}", "ffn_path": args.ffn_path,
                        "l2": "flushed between steps (512 MB write)",
                        "step": "whole layer replayed from a CUDA graph"},
             "roofline": roofline,
@@ -407,28 +415,39 @@ def measure_stream(L, dev, steps, warmup, rank):
     return out_d
 
 
-def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload):
+def ffn_path_used(P, E, path):
+    """The kernel the library runs for P pairs over E experts under path choice `path`."""
+    if path == "auto":
+        return "gemm" if P >= 32 * E else "gemv"
+    return path
+
+
+def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload, path="auto"):
     """Roofline of the expert FFN step (its two launches).  Few rows per expert: HBM-bound
-    grouped GEMV, algorithmic bytes = the selected experts' weights + activation rows.  Many
-    rows per expert: tensor-bound grouped GEMM, algorithmic flops = 2 * P * 3 * H * I."""
+    grouped GEMV (or decode GEMM), algorithmic bytes = the selected experts' weights +
+    activation rows.  Many rows per expert: tensor-bound grouped GEMM, algorithmic flops =
+    2 * P * 3 * H * I."""
     from quantized_expert_ffn_layer_b300 import ftmoe as F
     T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
     P = T * k
-    gemm = P >= 32 * E  # the library's automatic path choice
-    if not gemm:
+    used = ffn_path_used(P, E, path)
+    if used != "gemm":
         blob = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
         alg = U * blob + P * H * 2 + P * H * 2 + T * H * 2 + P * I * 2 * 2
         hbm = float(pk["hbm_gbs"])
         ach = alg / (ffn_ms / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "gemv_ffn_kernel x2 (gate/up+SwiGLU, down)",
+        name = ("gemv_ffn_kernel x2 (mma.sync; gate/up+SwiGLU, down)" if used == "gemv" else
+                "gemm_decode_kernel x2 (tcgen05, A in tensor memory; gate/up+SwiGLU, down)")
+        return {"bound": "hbm", "kernel": name, "path": used,
                 "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "peak_kind": f"{pk_kind} hbm_gbs (copy)",
-                "traffic": recorded_traffic("expert_ffn_gemv", workload),
+                "traffic": recorded_traffic("expert_ffn_" + used, workload),
                 "alg_bytes_per_launch": alg, "ms_per_launch": ffn_ms, "unique_experts": U}
     flops = 2.0 * P * 3 * H * I
     peak = float(pk["bf16_tflops"])
     ach = flops / (ffn_ms / 1e3) / 1e12
     return {"bound": "tensor", "kernel": "gemm_ffn_kernel x2 (tcgen05 kind::f16; gate/up+SwiGLU, down)",
+            "path": used,
             "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
             "peak_kind": f"{pk_kind} bf16_tflops (burst; the FFN is timed alone)",
             "traffic": recorded_traffic("expert_ffn_gemm", workload),

@@ -5,14 +5,16 @@
 // Decode reads every selected expert's weights once for a handful of tokens, so the
 // layer is bound by streaming the 4-bit weights from HBM, and what limits a kernel is
 // the number of instructions it spends per weight.  One persistent CTA per SM works
-// through items (expert, 128 weight rows, up to 16 of the expert's token rows): for
-// gate/up the gate and the up rows of 128 features (two A tiles), for down one 128-row
-// tile.  Per 64-element reduction slab ("stage"):
+// through items (expert, 2 x 128 weight rows, up to 16 of the expert's token rows): for
+// gate/up the gate and the up rows of 128 features, for down 256 output rows (two A
+// tiles either way).  Per 64-element reduction slab ("stage"):
 //   * a raw-weight warp keeps a deep ring of shared-memory slots filled with the
 //     stage's 4-bit weight records (one 1-D bulk copy per record row group and four
 //     stages) and warms L2 with the CTA's next item;
-//   * 8 converter warps turn each 16-row record into bf16 codes: q - 8 for Q4_0 (an
-//     integer in [-8, 7]) or the E2M1 value for MXFP4, both exact and unscaled.  Lane
+//   * 8 converter warps turn each 16-row record into exact, unscaled bf16 codes: the
+//     E2M1 value for MXFP4, 128 + q for Q4_0 (one byte permute per two weights; a
+//     constant A tile of -136 in tensor memory, multiplied into the same accumulator,
+//     turns every block sum into the sum of (q - 8) x).  Lane
 //     4g + c of a record holds elements 4c..4c+3 of every 16-element step for rows g
 //     and g + 8, which is exactly the thread layout of the 16x256b tensor-memory store,
 //     so every lane decodes its own 16 bytes and stores them without any exchange;
@@ -20,10 +22,13 @@
 //     for down) with cp.async into the 128-byte-swizzled K-major B tile;
 //   * one thread issues tcgen05.mma kind::f16 (A from tensor memory, B from shared
 //     memory, M = 128, N = 16, K = 16) into one fresh partial-sum accumulator per
-//     32-element quantization block;
+//     tile and 32-element quantization block;
 //   * 4 epilogue warps read the partial sums with tcgen05.ld and add block scale x
 //     partial sum into fp32 registers (one weight row per thread), then store
-//     h = silu(g) * u or y as bf16.
+//     h = silu(g) * u or y as bf16.  The converters copy each stage's block scales
+//     into a small ring of their own, so the raw ring is recycled as soon as the codes
+//     are decoded, and the token-row tiles have a deeper ring than the A stages, so
+//     neither waits on the latency of the MMAs.
 // So the only roundings are the fp32 sums, the bf16 h between the projections and the
 // bf16 output, as in the grouped GEMV.  The order of every sum is fixed and each output
 // depends only on its own weight row and token row, so a token's result does not depend
@@ -38,6 +43,7 @@
 namespace ftmoe {
 namespace dec {
 
+#define GD_WAIT mbar_wait_spin_or_abort
 constexpr int GD_TOK = 16;          // token rows per item (MMA N)
 constexpr int GD_ROWS = 128;        // weight rows per tile (MMA M, TMEM lanes)
 constexpr int GD_EPI_WARPS = 4;     // warps 0..3 (one per TMEM lane quarter)
@@ -52,32 +58,41 @@ constexpr int GD_STG = GD_TOK * 64;       // epilogue staging per warp: 16 rows 
 constexpr int GD_MAX_E = 1024;
 constexpr int GD_MAX_NR = 8;
 constexpr int GD_MAX_NS = 8;
+constexpr int GD_SC_REC = 64;             // scale bytes of one record (16 rows x 2 blocks)
 
 // Per-projection layout.  Tensor-memory columns: NPS partial-sum stages (per A tile
-// and quantization block, GD_TOK fp32 columns), then NS stages of A tiles (NT x 32
-// columns: 64 bf16 per lane).  The raw weight ring (shared memory) holds super-stages
+// and quantization block, GD_TOK fp32 columns), NS stages of A tiles (NT x 32 columns:
+// 64 bf16 per lane), then the constant -136 tile (8 columns: one k16 step).  The raw weight ring (shared memory) holds super-stages
 // of NKB consecutive slabs, filled with one bulk copy per record row group (the records
 // of a row group are contiguous along the reduction dimension).
 template <int MODE>
 struct GdCfg {
-  static constexpr int NT = MODE == 0 ? 2 : 1;            // A tiles (MMAs per k-step)
-  static constexpr int NS = MODE == 0 ? 4 : 8;            // A / B stages
-  static constexpr int NPS = MODE == 0 ? 4 : 8;           // partial-sum stages
-  static constexpr int LA = NS / 2;                       // token-row copy stages in flight
+  static constexpr int NT = 2;                            // A tiles (MMAs per k-step)
+  static constexpr int NS = 4;                            // A stages (tensor memory)
+  static constexpr int NPS = 3;                           // partial-sum stages
+  static constexpr int NSB = 8;                           // B stages (shared memory)
+  static constexpr int LA = 4;                            // token-row copy stages in flight
+  static constexpr int NSS = 8;                           // block-scale stages (shared memory)
   static constexpr int NKB = 4;                           // slabs per raw super-stage
-  static constexpr int NR = MODE == 0 ? 4 : 6;            // raw weight super-stages
+  static constexpr int NR = 4;                            // raw weight super-stages
   static constexpr int NREC = 8 * NT;                     // weight records per stage
   static constexpr int RAW_STAGE = NREC * NKB * 576;      // [record][slab][576]
   static constexpr int PS_STAGE_COLS = NT * 2 * GD_TOK;   // [tile][block][token]
   static constexpr int A_COL0 = NPS * PS_STAGE_COLS;
+  static constexpr int CONST_COL = A_COL0 + NS * NT * 32;  // 128 lanes x 16 bf16 of -136
   static constexpr int A_STAGE_COLS = NT * 32;
-  static_assert(A_COL0 + NS * A_STAGE_COLS <= (int)GD_TMEM_COLS, "tensor memory columns");
-  static_assert(NS <= GD_MAX_NS && NPS <= GD_MAX_NS && NR <= GD_MAX_NR && LA >= 1, "ring sizes");
+  static_assert(CONST_COL + 8 <= (int)GD_TMEM_COLS, "tensor memory columns");
+  static_assert(NS <= GD_MAX_NS && NPS <= GD_MAX_NS && NSB <= GD_MAX_NS && NSS <= GD_MAX_NS &&
+                    NR <= GD_MAX_NR && LA >= 1 && LA < NSB, "ring sizes");
+  // A converter overwrites scale slot s % NSS only after the MMA of stage s - NS has
+  // completed, which needed the epilogue to be done with stage s - NS - NPS: so the
+  // slot's previous stage (s - NSS) has been read.
+  static_assert(NSS > NS + NPS, "scale ring must outlast the A and partial-sum rings");
 };
 
 struct GdTail {
   uint64_t raw_full[GD_MAX_NR], raw_empty[GD_MAX_NR];
-  uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS];
+  uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS], b_empty[GD_MAX_NS], sc_full[GD_MAX_NS];
   uint64_t ps_full[GD_MAX_NS], ps_empty[GD_MAX_NS], drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -85,8 +100,9 @@ struct GdTail {
 };
 template <int MODE>
 constexpr size_t gd_smem_bytes() {
-  return 1024 + (size_t)GdCfg<MODE>::NS * GD_B_TILE + (size_t)GdCfg<MODE>::NR * GdCfg<MODE>::RAW_STAGE +
-         (size_t)GD_EPI_WARPS * GD_STG + sizeof(GdTail);
+  return 1024 + (size_t)GdCfg<MODE>::NSB * GD_B_TILE + (size_t)GdCfg<MODE>::NR * GdCfg<MODE>::RAW_STAGE +
+         (size_t)GdCfg<MODE>::NSS * GdCfg<MODE>::NREC * GD_SC_REC + (size_t)GD_EPI_WARPS * GD_STG +
+         sizeof(GdTail);
 }
 
 
@@ -140,16 +156,18 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   const int ft = local / ntt, tt = local - ft * ntt;
   it.r0 = beg + tt * GD_TOK;
   it.n = min(GD_TOK, ne - tt * GD_TOK);
-  it.f0 = ft * GD_ROWS;
+  it.f0 = ft * (MODE == 0 ? GD_ROWS : 2 * GD_ROWS);
   return it;
 }
 
 // First matrix row of record ri (tile ri / 8, 16-row group ri % 8) of an item, and
-// whether that row group lies inside the projection's result rows.
+// whether that row group lies inside the projection's result rows.  Gate/up: tile 0
+// holds the gate rows and tile 1 the up rows of the same features; down: tile 1 holds
+// the 128 rows after tile 0's.
 template <int MODE>
 __device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const GemmArgs& a,
                                              bool& ok) {
-  const int row = it.f0 + (ri & 7) * 16;
+  const int row = it.f0 + (MODE == 1 ? (ri >> 3) * GD_ROWS : 0) + (ri & 7) * 16;
   ok = row < a.nrows;
   return (MODE == 0 && (ri >> 3)) ? row + a.up_row0 : row;
 }
@@ -184,17 +202,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
 
 // bf16x2 codes of elements (0, 1) and (2, 3) of a 4-element group from a word whose
 // bytes hold the group's 4-bit codes in the order (e0, e2, e1, e3), one per low nibble:
-// q - 8 for Q4_0, the E2M1 value for MXFP4.  Both are exact in bf16.
+// 128 + q for Q4_0 (the byte 0x43 above a code byte is bf16 128 + q), the E2M1 value
+// for MXFP4.  Both are exact in bf16.
 template <int QT>
 __device__ __forceinline__ void decode_plain(uint32_t E, uint32_t& o0, uint32_t& o1) {
   if (QT == FTMOE_Q4_0) {
-    const uint32_t K = 0x43434343u;  // high byte of bf16 128: (128 + q) per element
-    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-    uint32_t t0 = prmt(E, K, 0x4240u), t1 = prmt(E, K, 0x4341u);
-    const __nv_bfloat162 u0 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t0), off);
-    const __nv_bfloat162 u1 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t1), off);
-    o0 = *reinterpret_cast<const uint32_t*>(&u0);
-    o1 = *reinterpret_cast<const uint32_t*>(&u1);
+    const uint32_t K = 0x43434343u;
+    o0 = prmt(E, K, 0x4240u);
+    o1 = prmt(E, K, 0x4341u);
   } else {
     const uint32_t TWO126 = 0x7E807E80u;
     const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
@@ -232,14 +247,16 @@ __device__ __forceinline__ void convert_record(uint32_t rec, uint32_t taddr, int
   tmem_st_16x256b_x4(taddr, out);
 }
 
-// Block scale of weight row g + 8 h of a record for quantization block b, as fp32.
+// Block scale of weight row g + 8 h for quantization block b, as fp32, from a copy of
+// a record's scale bytes at `sc` (per row group g: (g, b0), (g + 8, b0), (g, b1),
+// (g + 8, b1), fp16 for Q4_0, E8M0 for MXFP4).
 template <int QT>
-__device__ __forceinline__ float record_scale(uint32_t rec, int g, int h, int b) {
+__device__ __forceinline__ float block_scale(uint32_t sc, int g, int h, int b) {
   if (QT == FTMOE_Q4_0) {
-    const uint32_t wd = lds32(rec + REC_CODE_BYTES + g * 8 + b * 4);
+    const uint32_t wd = lds32(sc + g * 8 + b * 4);
     return half_bits_to_f32(h ? (wd >> 16) : (wd & 0xFFFFu));
   } else {
-    const uint32_t wd = lds32(rec + REC_CODE_BYTES + g * 4);
+    const uint32_t wd = lds32(sc + g * 4);
     return e8m0_to_f32((wd >> (8 * (2 * b + h))) & 0xFFu);
   }
 }
@@ -269,10 +286,11 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // B stages (128-byte swizzle)
   uint8_t* base = smem_raw + (base_addr - raw_addr);
-  const uint32_t rawring = base_addr + C::NS * GD_B_TILE;
-  const uint32_t staging = rawring + C::NR * C::RAW_STAGE;
-  GdTail& tl = *reinterpret_cast<GdTail*>(base + (size_t)C::NS * GD_B_TILE +
-                                          (size_t)C::NR * C::RAW_STAGE + GD_EPI_WARPS * GD_STG);
+  const uint32_t rawring = base_addr + C::NSB * GD_B_TILE;
+  const uint32_t scring = rawring + C::NR * C::RAW_STAGE;  // [NSS][NREC][64] block scales
+  const uint32_t staging = scring + C::NSS * C::NREC * GD_SC_REC;
+  GdTail& tl = *reinterpret_cast<GdTail*>(base + (size_t)C::NSB * GD_B_TILE + (size_t)C::NR * C::RAW_STAGE +
+                                          (size_t)C::NSS * C::NREC * GD_SC_REC + GD_EPI_WARPS * GD_STG);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &tl.abort_flag;
 
@@ -280,12 +298,14 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < C::NR; ++s) {
       mbar_init(&tl.raw_full[s], 1);
-      mbar_init(&tl.raw_empty[s], GD_CONV_WARPS + GD_EPI_WARPS);  // codes and scales read
+      mbar_init(&tl.raw_empty[s], GD_CONV_WARPS);
     }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&tl.a_full[s], GD_CONV_WARPS);
       mbar_init(&tl.empty[s], 1);
     }
+    for (int s = 0; s < C::NSB; ++s) mbar_init(&tl.b_empty[s], 1);
+    for (int s = 0; s < C::NSS; ++s) mbar_init(&tl.sc_full[s], GD_CONV_WARPS);
     for (int s = 0; s < C::NPS; ++s) {
       mbar_init(&tl.ps_full[s], 1);
       mbar_init(&tl.ps_empty[s], GD_EPI_WARPS);
@@ -319,8 +339,19 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  pdl_launch_dependents();
   const uint32_t tmem = tl.tmem_base;
+  if (QT == FTMOE_Q4_0 && warp < GD_EPI_WARPS) {
+    // the constant A tile: -136 (bf16 0xC308) in every lane and element
+    uint32_t c8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c8[j] = 0xC308C308u;
+    tmem_st8(tmem + ((uint32_t)(32 * warp) << 16) + C::CONST_COL, c8);
+    tmem_wait_st();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  pdl_launch_dependents();
   const int nitems = tl.citem[a.E];
   const int G = gridDim.x;
 
@@ -345,11 +376,11 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       }
       for (int kb0 = 0; kb0 < a.S; kb0 += C::NKB) {
         const int nkb = min(C::NKB, a.S - kb0);
-        if (!mbar_wait_or_abort(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
+        if (!GD_WAIT(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
         if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * nkb * RB));
         __syncwarp();
         if (lane < C::NREC && rok)
-          bulk_g2s(base + C::NS * GD_B_TILE + rslot * C::RAW_STAGE + lane * (C::NKB * RB),
+          bulk_g2s(base + C::NSB * GD_B_TILE + rslot * C::RAW_STAGE + lane * (C::NKB * RB),
                    rec0 + (long long)kb0 * RB, (uint32_t)(nkb * RB), &tl.raw_full[rslot]);
         if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
       }
@@ -361,8 +392,9 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     const int cw = ct >> 5;          // converter warp; its TMEM lane quarter = cw % 4
     const int grp = 2 * (cw & 3) + (cw >> 2);  // record row group: TMEM lanes 16 grp ..
     const uint32_t tlane = tmem + ((uint32_t)(16 * grp) << 16) + C::A_COL0;
-    int slot = 0, rslot = 0;
+    int slot = 0, rslot = 0, sslot = 0;
     uint32_t phase = 0, rphase = 0;
+    constexpr int SCB = QT == FTMOE_Q4_0 ? 64 : 32;  // scale bytes per record
     // token rows: threads ct < GD_TOK * 8 copy 16-byte chunk (ct & 7) of row ct >> 3, LA
     // stages ahead of the conversion so that the copies' latency hides behind the decode.
     // Every call commits one cp.async group (empty past the last stage), so that waiting
@@ -380,7 +412,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       }
     };
     auto issue_rows = [&]() {  // copies of stage (bi, bkb)
-      if (bi >= nitems || !mbar_wait_or_abort(&tl.empty[bslot], bphase ^ 1u, abort_flag, a.status)) {
+      if (bi >= nitems || !GD_WAIT(&tl.b_empty[bslot], bphase ^ 1u, abort_flag, a.status)) {
         cp_async_commit();
         return;
       }
@@ -391,7 +423,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
                    kok ? rowp + bkb * 64 : rowp, kok ? 16u : 0u);
       }
       cp_async_commit();
-      if (++bslot == C::NS) { bslot = 0; bphase ^= 1u; }
+      if (++bslot == C::NSB) { bslot = 0; bphase ^= 1u; }
       if (++bkb == a.S) {
         bkb = 0;
         bi += G;
@@ -403,32 +435,42 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     for (int s = 0; s < C::LA; ++s) issue_rows();
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
-      bool rok;
-      gm_record_row<MODE>(it, grp, a, rok);  // the same row group in every tile
+      bool rok[C::NT];
+#pragma unroll
+      for (int t = 0; t < C::NT; ++t) gm_record_row<MODE>(it, t * 8 + grp, a, rok[t]);
       for (int kb = 0; kb < a.S; ++kb) {
         const int jkb = kb % C::NKB;  // slab within the raw super-stage
         const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
         issue_rows();
-        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
-        if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+        if (!GD_WAIT(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
+        if (!GD_WAIT(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
-        if (rok) {
 #pragma unroll
-          for (int t = 0; t < C::NT; ++t)
-            convert_record<QT>(rawring + rslot * C::RAW_STAGE + ((t * 8 + grp) * C::NKB + jkb) * RB,
-                               tlane + slot * C::A_STAGE_COLS + t * 32, lane);
-          tmem_wait_st();
+        for (int t = 0; t < C::NT; ++t) {  // (records outside the result rows are left as they are)
+          const uint32_t rec = rawring + rslot * C::RAW_STAGE + ((t * 8 + grp) * C::NKB + jkb) * RB;
+          if (rok[t]) {
+            convert_record<QT>(rec, tlane + slot * C::A_STAGE_COLS + t * 32, lane);
+            // the record's block scales go to the scale ring for the epilogue
+            if (lane < SCB / 4)
+              asm volatile("st.shared.u32 [%0], %1;" ::"r"(scring + (sslot * C::NREC + t * 8 + grp) * GD_SC_REC +
+                                                          lane * 4),
+                           "r"(lds32(rec + REC_CODE_BYTES + lane * 4))
+                           : "memory");
+          }
         }
+        tmem_wait_st();
         cp_async_wait<C::LA>();  // this stage's rows have landed
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
           if (last_of_super) mbar_arrive(&tl.raw_empty[rslot]);
+          mbar_arrive(&tl.sc_full[sslot]);
           mbar_arrive(&tl.a_full[slot]);
         }
         if (last_of_super && ++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
         if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+        if (++sslot == C::NSS) sslot = 0;
       }
       if (*abort_flag) break;
     }
@@ -436,32 +478,37 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   } else if (warp == GD_MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      int slot = 0, ps = 0;
+      int slot = 0, ps = 0, bslot = 0;
       uint32_t phase = 0, pphase = 0;
       const uint32_t idesc = idesc_bf16_f32(GD_ROWS, GD_TOK);
       bool ok = true;
       for (int i = blockIdx.x; i < nitems && ok; i += G) {
         for (int kb = 0; kb < a.S; ++kb) {
-          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status) ||
-              !mbar_wait_or_abort(&tl.ps_empty[ps], pphase ^ 1u, abort_flag, a.status)) {
+          if (!GD_WAIT(&tl.a_full[slot], phase, abort_flag, a.status) ||
+              !GD_WAIT(&tl.ps_empty[ps], pphase ^ 1u, abort_flag, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t bs = base_addr + slot * GD_B_TILE;
+          const uint32_t bs = base_addr + bslot * GD_B_TILE;
           const uint32_t as = tmem + C::A_COL0 + slot * C::A_STAGE_COLS;
           const uint32_t pd = tmem + ps * C::PS_STAGE_COLS;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // k16 step; block kk / 2 starts from zero
             const uint64_t bd = sdesc_kmajor_sw128(bs + 32 * kk);
 #pragma unroll
-            for (int t = 0; t < C::NT; ++t)
-              mma_bf16_tmem_a(pd + (t * 2 + (kk >> 1)) * GD_TOK, as + t * 32 + 8 * kk, bd, idesc,
-                              (uint32_t)(kk & 1));
+            for (int t = 0; t < C::NT; ++t) {
+              const uint32_t d = pd + (t * 2 + (kk >> 1)) * GD_TOK;
+              mma_bf16_tmem_a(d, as + t * 32 + 8 * kk, bd, idesc, (uint32_t)(kk & 1));
+              // Q4_0 codes are 128 + q: add -136 x the same 16 token columns
+              if (QT == FTMOE_Q4_0) mma_bf16_tmem_a(d, tmem + C::CONST_COL, bd, idesc, 1u);
+            }
           }
           mma_commit(&tl.empty[slot]);
+          mma_commit(&tl.b_empty[bslot]);
           mma_commit(&tl.ps_full[ps]);
           if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+          if (++bslot == C::NSB) bslot = 0;
           if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
         }
       }
@@ -479,8 +526,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     // lanes l and l ^ 1 hold adjacent features: they swap values to store bf16 pairs
     const int odd = lane & 1;
     const uint32_t stg = staging + q * GD_STG;
-    int ps = 0, rslot = 0;
-    uint32_t pphase = 0, rphase = 0;
+    int ps = 0, sslot = 0;
+    uint32_t pphase = 0, sphase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       const int nch = (it.n + 3) >> 2;  // 4-token chunks with real tokens
@@ -491,12 +538,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
         for (int j = 0; j < GD_TOK; ++j) acc[t][j] = 0.f;
       bool ok = true;
       for (int kb = 0; kb < a.S; ++kb) {
-        const int jkb = kb % C::NKB;
-        const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
-        // (the raw slot is already full: the wait only orders its scale bytes before
-        // the reads below)
-        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status) ||
-            !mbar_wait_or_abort(&tl.ps_full[ps], pphase, abort_flag, a.status)) {
+        if (!GD_WAIT(&tl.sc_full[sslot], sphase, abort_flag, a.status) ||
+            !GD_WAIT(&tl.ps_full[ps], pphase, abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -504,9 +547,9 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
         const bool b1 = kb * 64 + 32 < a.K;  // the slab's second block lies inside K
 #pragma unroll
         for (int t = 0; t < C::NT; ++t) {
-          const uint32_t rec = rawring + rslot * C::RAW_STAGE + ((t * 8 + grp) * C::NKB + jkb) * RB;
-          const float d0 = record_scale<QT>(rec, g, h, 0);
-          const float d1 = b1 ? record_scale<QT>(rec, g, h, 1) : 0.f;
+          const uint32_t sc = scring + (sslot * C::NREC + t * 8 + grp) * GD_SC_REC;
+          const float d0 = block_scale<QT>(sc, g, h, 0);
+          const float d1 = b1 ? block_scale<QT>(sc, g, h, 1) : 0.f;
           uint32_t p0[GD_TOK], p1[GD_TOK];
           const uint32_t pc = lane_base + ps * C::PS_STAGE_COLS + t * 2 * GD_TOK;
           tmem_ld16(pc, p0);
@@ -525,48 +568,48 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tl.ps_empty[ps]);
-          if (last_of_super) mbar_arrive(&tl.raw_empty[rslot]);
-        }
-        if (last_of_super && ++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+        if (lane == 0) mbar_arrive(&tl.ps_empty[ps]);
+        if (++sslot == C::NSS) { sslot = 0; sphase ^= 1u; }
         if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
       }
       if (!ok) break;
-      // ---- item result: h = silu(gate) * up, or y; row r of the tile for tokens 0..n-1.
-      // The warp's 32 features x 16 tokens go through its staging tile [token][feature]
-      // so that the global stores are 16-byte vectors.
-      float v[GD_TOK];
+      // ---- item result: h = silu(gate) * up (one output tile), or y (two); row r of each
+      // output tile for tokens 0..n-1.  The warp's 32 features x 16 tokens go through its
+      // staging tile [token][feature] so that the global stores are 16-byte vectors.
 #pragma unroll
-      for (int j = 0; j < GD_TOK; ++j) {
-        if (MODE == 0) {
-          const float gg = acc[0][j];
-          v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * acc[C::NT - 1][j];
-        } else {
-          v[j] = acc[0][j];
+      for (int ot = 0; ot < (MODE == 0 ? 1 : C::NT); ++ot) {
+        float v[GD_TOK];
+#pragma unroll
+        for (int j = 0; j < GD_TOK; ++j) {
+          if (MODE == 0) {
+            const float gg = acc[0][j];
+            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * acc[1][j];
+          } else {
+            v[j] = acc[ot][j];
+          }
         }
-      }
-      const int fw = it.f0 + 32 * q;  // first feature of this warp
-      const bool fok = fw < a.nrows;
-      uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
+        const int fw = it.f0 + ot * GD_ROWS + 32 * q;  // first feature of this warp
+        const bool fok = fw < a.nrows;
+        uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
 #pragma unroll
-      for (int p = 0; p < GD_TOK / 2; ++p) {
-        const float send = odd ? v[2 * p] : v[2 * p + 1];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-        const float lo = odd ? recv : v[2 * p];
-        const float hi = odd ? v[2 * p + 1] : recv;
-        const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (lane & ~1) * 2), "r"(w)
-                     : "memory");
-      }
-      __syncwarp();
+        for (int p = 0; p < GD_TOK / 2; ++p) {
+          const float send = odd ? v[2 * p] : v[2 * p + 1];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          const float lo = odd ? recv : v[2 * p];
+          const float hi = odd ? v[2 * p + 1] : recv;
+          const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (lane & ~1) * 2), "r"(w)
+                       : "memory");
+        }
+        __syncwarp();
 #pragma unroll
-      for (int r4 = 0; r4 < GD_TOK / 8; ++r4) {
-        const int row = 8 * r4 + (lane >> 2);
-        const uint4 d = lds128(stg + row * 64 + (lane & 3) * 16);
-        if (fok && row < it.n) *reinterpret_cast<uint4*>(obase + (long long)row * a.out_ld) = d;
+        for (int r4 = 0; r4 < GD_TOK / 8; ++r4) {
+          const int row = 8 * r4 + (lane >> 2);
+          const uint4 d = lds128(stg + row * 64 + (lane & 3) * 16);
+          if (fok && row < it.n) *reinterpret_cast<uint4*>(obase + (long long)row * a.out_ld) = d;
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   }
 
@@ -634,7 +677,7 @@ static cudaError_t gd_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   d.S = slabs_of(pb.I);
   d.nrows = pb.H;
   d.up_row0 = 0;
-  d.ft_per_expert = (pb.H + GD_ROWS - 1) / GD_ROWS;
+  d.ft_per_expert = (pb.H + 2 * GD_ROWS - 1) / (2 * GD_ROWS);
   cudaError_t err = gd_launch<QT, 0>(a, tab, st);
   if (err != cudaSuccess) return err;
   return gd_launch<QT, 1>(d, tab, st);

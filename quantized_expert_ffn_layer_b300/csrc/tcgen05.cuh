@@ -186,4 +186,24 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
   }
 }
 
+// Same contract as mbar_wait_or_abort, but polls without a suspend hint (the thread
+// stays runnable), for roles whose per-stage work is short next to a wake-up.
+__device__ __forceinline__ bool mbar_wait_spin_or_abort(uint64_t* bar, uint32_t parity,
+                                                        volatile int* abort_flag, int* status,
+                                                        uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      set_device_code(status, DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 }  // namespace ftmoe

@@ -418,7 +418,7 @@ def measure_stream(L, dev, steps, warmup, rank):
 def ffn_path_used(P, E, path):
     """The kernel the library runs for P pairs over E experts under path choice `path`."""
     if path == "auto":
-        return "gemm" if P >= 32 * E else "gemv"
+        return "gemm" if P >= 32 * E else ("gemm_decode" if P >= 8 * E else "gemv")
     return path
 
 

@@ -70,10 +70,10 @@ typedef enum { FTMOE_Q4_0 = 1, FTMOE_MXFP4 = 2 } ftmoe_qtype;
 
 /* Expert FFN path selection (ftmoe_set_ffn_path). */
 typedef enum {
-  FTMOE_PATH_AUTO = 0,        /* GEMM when rows >= 32 * E, GEMV otherwise */
+  FTMOE_PATH_AUTO = 0,        /* GEMV below 8 E rows, GEMM_DECODE below 32 E, else GEMM */
   FTMOE_PATH_GEMV = 1,        /* grouped GEMV on mma.sync with split reductions for tiny batches */
   FTMOE_PATH_GEMM = 2,        /* tcgen05 grouped GEMM, 256-token tiles, bf16 weights staged in smem */
-  FTMOE_PATH_GEMM_DECODE = 3  /* tcgen05 grouped GEMM, 32-token tiles, bf16 weights in tensor memory */
+  FTMOE_PATH_GEMM_DECODE = 3  /* tcgen05 grouped GEMM, 16-token tiles, codes in tensor memory */
 } ftmoe_path;
 
 /* Human-readable name of a status code (static string; never NULL). */
@@ -193,12 +193,12 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_weights* wts, const uint16_t* x, int T
                               const int32_t* offsets, const int32_t* sorted_pair,
                               uint16_t* y_perm, void* ws, size_t ws_bytes, ftmoe_stream_t stream);
 
-/* Kernel choice for ftmoe_expert_ffn / ftmoe_layer (ftmoe_path): AUTO picks
- * GEMM when T * k >= 32 E and GEMV otherwise; GEMM_DECODE is only used when asked
- * for.  Every path computes the same
- * definition; the reduction order (and so the last bits) differs between paths, but
- * within one path a token's output does not depend on the other tokens of the batch.
- * Process-wide setting; returns the previous value. */
+/* Kernel choice for ftmoe_expert_ffn / ftmoe_layer (ftmoe_path): AUTO picks the
+ * GEMV when T * k < 8 E, GEMM_DECODE when 8 E <= T * k < 32 E and GEMM otherwise
+ * (the crossovers measured on the decode layer shape).  Every path computes the
+ * same definition; the reduction order (and so the last bits) differs between
+ * paths, but within one path a token's output does not depend on the other tokens
+ * of the batch.  Process-wide setting; returns the previous value. */
 int ftmoe_set_ffn_path(int path);
 
 /* ------------------------------------------------------------------ combine

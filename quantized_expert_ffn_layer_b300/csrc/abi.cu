@@ -111,18 +111,21 @@ ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, 
   FfnWs fw = carve_ffn(ws, T, k, E, wts->H, wts->I);
   pb.h_act = fw.h_act;
   const int path = g_ffn_path;
+  // measured crossovers (decode layer shape on B300): the grouped GEMV wins below about
+  // 8 rows per expert, the decode GEMM between 8 and 32, the prefill GEMM above
   const bool many_rows = (long long)pb.P >= 32LL * E;
+  const bool mid_rows = (long long)pb.P >= 8LL * E;
   if (path == FTMOE_PATH_GEMM || (path == FTMOE_PATH_AUTO && many_rows)) {
     cudaError_t e = launch_ffn_gemm(pb, fw.gemm_ws, fw.gemm_bytes, st);
     if (e == cudaSuccess) return FTMOE_OK;
     if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
     if (path == FTMOE_PATH_GEMM) return FTMOE_ERR_UNSUPPORTED;
   }
-  if (path == FTMOE_PATH_GEMM_DECODE) {
+  if (path == FTMOE_PATH_GEMM_DECODE || (path == FTMOE_PATH_AUTO && mid_rows)) {
     cudaError_t e = launch_ffn_gemm_decode(pb, st);
     if (e == cudaSuccess) return FTMOE_OK;
     if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
-    return FTMOE_ERR_UNSUPPORTED;
+    if (path == FTMOE_PATH_GEMM_DECODE) return FTMOE_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_ffn_gemv(pb, fw.gemv_ws, ws_zeroed, st));
 }

@@ -11,10 +11,8 @@
 //   * a raw-weight warp keeps a deep ring of shared-memory slots filled with the
 //     stage's 4-bit weight records (one 1-D bulk copy per record row group and four
 //     stages) and warms L2 with the CTA's next item;
-//   * 8 converter warps turn each 16-row record into exact, unscaled bf16 codes: the
-//     E2M1 value for MXFP4, 128 + q for Q4_0 (one byte permute per two weights; a
-//     constant A tile of -136 in tensor memory, multiplied into the same accumulator,
-//     turns every block sum into the sum of (q - 8) x).  Lane
+//   * 8 converter warps turn each 16-row record into exact, unscaled bf16 codes: q - 8
+//     for Q4_0 (an integer in [-8, 7]), the E2M1 value for MXFP4.  Lane
 //     4g + c of a record holds elements 4c..4c+3 of every 16-element step for rows g
 //     and g + 8, which is exactly the thread layout of the 16x256b tensor-memory store,
 //     so every lane decodes its own 16 bytes and stores them without any exchange;
@@ -61,8 +59,8 @@ constexpr int GD_MAX_NS = 8;
 constexpr int GD_SC_REC = 64;             // scale bytes of one record (16 rows x 2 blocks)
 
 // Per-projection layout.  Tensor-memory columns: NPS partial-sum stages (per A tile
-// and quantization block, GD_TOK fp32 columns), NS stages of A tiles (NT x 32 columns:
-// 64 bf16 per lane), then the constant -136 tile (8 columns: one k16 step).  The raw weight ring (shared memory) holds super-stages
+// and quantization block, GD_TOK fp32 columns), then NS stages of A tiles (NT x 32
+// columns: 64 bf16 per lane).  The raw weight ring (shared memory) holds super-stages
 // of NKB consecutive slabs, filled with one bulk copy per record row group (the records
 // of a row group are contiguous along the reduction dimension).
 template <int MODE>
@@ -71,7 +69,7 @@ struct GdCfg {
   static constexpr int NS = 4;                            // A stages (tensor memory)
   static constexpr int NPS = 3;                           // partial-sum stages
   static constexpr int NSB = 8;                           // B stages (shared memory)
-  static constexpr int LA = 4;                            // token-row copy stages in flight
+  static constexpr int LA = NSB - NS;                     // token-row copy stages in flight
   static constexpr int NSS = 8;                           // block-scale stages (shared memory)
   static constexpr int NKB = 4;                           // slabs per raw super-stage
   static constexpr int NR = 4;                            // raw weight super-stages
@@ -79,21 +77,27 @@ struct GdCfg {
   static constexpr int RAW_STAGE = NREC * NKB * 576;      // [record][slab][576]
   static constexpr int PS_STAGE_COLS = NT * 2 * GD_TOK;   // [tile][block][token]
   static constexpr int A_COL0 = NPS * PS_STAGE_COLS;
-  static constexpr int CONST_COL = A_COL0 + NS * NT * 32;  // 128 lanes x 16 bf16 of -136
   static constexpr int A_STAGE_COLS = NT * 32;
-  static_assert(CONST_COL + 8 <= (int)GD_TMEM_COLS, "tensor memory columns");
+  static_assert(A_COL0 + NS * A_STAGE_COLS <= (int)GD_TMEM_COLS, "tensor memory columns");
   static_assert(NS <= GD_MAX_NS && NPS <= GD_MAX_NS && NSB <= GD_MAX_NS && NSS <= GD_MAX_NS &&
                     NR <= GD_MAX_NR && LA >= 1 && LA < NSB, "ring sizes");
-  // A converter overwrites scale slot s % NSS only after the MMA of stage s - NS has
-  // completed, which needed the epilogue to be done with stage s - NS - NPS: so the
-  // slot's previous stage (s - NSS) has been read.
+  // One MMA commit per stage (on empty[s % NS]) serves every consumer:
+  //  * converters wait for the MMAs of stage s - NS before writing A slot s % NS, and
+  //    then copy the token rows of stage s + LA into B slot (s + LA) % NSB, whose last
+  //    user was stage s + LA - NSB = s - NS;
+  //  * the epilogue waits for the MMAs of stage s itself on the same barrier; the MMAs
+  //    of stage s + NS cannot complete before the epilogue is done with stage
+  //    s + NS - NPS > s (partial-sum ring), so the barrier is never two phases ahead;
+  //  * a converter overwrites scale slot s % NSS only after the MMAs of stage s - NS
+  //    completed, which needed the epilogue done with stage s - NS - NPS, so the slot's
+  //    previous stage (s - NSS) has been read.
+  static_assert(NPS < NS, "partial-sum ring shorter than the A ring");
   static_assert(NSS > NS + NPS, "scale ring must outlast the A and partial-sum rings");
 };
 
 struct GdTail {
   uint64_t raw_full[GD_MAX_NR], raw_empty[GD_MAX_NR];
-  uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS], b_empty[GD_MAX_NS], sc_full[GD_MAX_NS];
-  uint64_t ps_full[GD_MAX_NS], ps_empty[GD_MAX_NS], drain;
+  uint64_t a_full[GD_MAX_NS], empty[GD_MAX_NS], sc_full[GD_MAX_NS], ps_empty[GD_MAX_NS], drain;
   uint32_t tmem_base;
   int abort_flag;
   int citem[GD_MAX_E + 1];  // exclusive prefix of items per expert
@@ -202,14 +206,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
 
 // bf16x2 codes of elements (0, 1) and (2, 3) of a 4-element group from a word whose
 // bytes hold the group's 4-bit codes in the order (e0, e2, e1, e3), one per low nibble:
-// 128 + q for Q4_0 (the byte 0x43 above a code byte is bf16 128 + q), the E2M1 value
-// for MXFP4.  Both are exact in bf16.
+// q - 8 for Q4_0 (the byte 0x43 above a code byte is bf16 128 + q; one bf16x2 subtract
+// of 136), the E2M1 value for MXFP4.  Both are exact in bf16.
 template <int QT>
 __device__ __forceinline__ void decode_plain(uint32_t E, uint32_t& o0, uint32_t& o1) {
   if (QT == FTMOE_Q4_0) {
     const uint32_t K = 0x43434343u;
-    o0 = prmt(E, K, 0x4240u);
-    o1 = prmt(E, K, 0x4341u);
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+    uint32_t t0 = prmt(E, K, 0x4240u), t1 = prmt(E, K, 0x4341u);
+    const __nv_bfloat162 u0 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t0), off);
+    const __nv_bfloat162 u1 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t1), off);
+    o0 = *reinterpret_cast<const uint32_t*>(&u0);
+    o1 = *reinterpret_cast<const uint32_t*>(&u1);
   } else {
     const uint32_t TWO126 = 0x7E807E80u;
     const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
@@ -304,12 +312,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       mbar_init(&tl.a_full[s], GD_CONV_WARPS);
       mbar_init(&tl.empty[s], 1);
     }
-    for (int s = 0; s < C::NSB; ++s) mbar_init(&tl.b_empty[s], 1);
     for (int s = 0; s < C::NSS; ++s) mbar_init(&tl.sc_full[s], GD_CONV_WARPS);
-    for (int s = 0; s < C::NPS; ++s) {
-      mbar_init(&tl.ps_full[s], 1);
-      mbar_init(&tl.ps_empty[s], GD_EPI_WARPS);
-    }
+    for (int s = 0; s < C::NPS; ++s) mbar_init(&tl.ps_empty[s], GD_EPI_WARPS);
     mbar_init(&tl.drain, 1);
     tl.abort_flag = 0;
     fence_barrier_init();
@@ -340,17 +344,6 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tl.tmem_base;
-  if (QT == FTMOE_Q4_0 && warp < GD_EPI_WARPS) {
-    // the constant A tile: -136 (bf16 0xC308) in every lane and element
-    uint32_t c8[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) c8[j] = 0xC308C308u;
-    tmem_st8(tmem + ((uint32_t)(32 * warp) << 16) + C::CONST_COL, c8);
-    tmem_wait_st();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
   pdl_launch_dependents();
   const int nitems = tl.citem[a.E];
   const int G = gridDim.x;
@@ -401,7 +394,6 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     // for all but the newest LA groups always means "this stage's rows have landed".
     const int brow = ct >> 3, ch = ct & 7;
     int bi = blockIdx.x, bkb = 0, bslot = 0;
-    uint32_t bphase = 0;
     const uint16_t* rowp = nullptr;
     auto load_rows = [&](int item) {
       const GmItem it = gm_item<MODE>(item, a, tl.citem);
@@ -411,8 +403,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
         rowp = a.act + ar * a.act_ld + ch * 8;
       }
     };
-    auto issue_rows = [&]() {  // copies of stage (bi, bkb)
-      if (bi >= nitems || !GD_WAIT(&tl.b_empty[bslot], bphase ^ 1u, abort_flag, a.status)) {
+    auto issue_rows = [&]() {  // copies of stage (bi, bkb); its B slot is free (see GdCfg)
+      if (bi >= nitems) {
         cp_async_commit();
         return;
       }
@@ -423,7 +415,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
                    kok ? rowp + bkb * 64 : rowp, kok ? 16u : 0u);
       }
       cp_async_commit();
-      if (++bslot == C::NSB) { bslot = 0; bphase ^= 1u; }
+      if (++bslot == C::NSB) bslot = 0;
       if (++bkb == a.S) {
         bkb = 0;
         bi += G;
@@ -441,9 +433,9 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       for (int kb = 0; kb < a.S; ++kb) {
         const int jkb = kb % C::NKB;  // slab within the raw super-stage
         const bool last_of_super = jkb == C::NKB - 1 || kb == a.S - 1;
+        if (!GD_WAIT(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         issue_rows();
         if (!GD_WAIT(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
-        if (!GD_WAIT(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int t = 0; t < C::NT; ++t) {  // (records outside the result rows are left as they are)
@@ -500,13 +492,9 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
             for (int t = 0; t < C::NT; ++t) {
               const uint32_t d = pd + (t * 2 + (kk >> 1)) * GD_TOK;
               mma_bf16_tmem_a(d, as + t * 32 + 8 * kk, bd, idesc, (uint32_t)(kk & 1));
-              // Q4_0 codes are 128 + q: add -136 x the same 16 token columns
-              if (QT == FTMOE_Q4_0) mma_bf16_tmem_a(d, tmem + C::CONST_COL, bd, idesc, 1u);
             }
           }
           mma_commit(&tl.empty[slot]);
-          mma_commit(&tl.b_empty[bslot]);
-          mma_commit(&tl.ps_full[ps]);
           if (++slot == C::NS) { slot = 0; phase ^= 1u; }
           if (++bslot == C::NSB) bslot = 0;
           if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
@@ -526,8 +514,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     // lanes l and l ^ 1 hold adjacent features: they swap values to store bf16 pairs
     const int odd = lane & 1;
     const uint32_t stg = staging + q * GD_STG;
-    int ps = 0, sslot = 0;
-    uint32_t pphase = 0, sphase = 0;
+    int ps = 0, sslot = 0, eslot = 0;
+    uint32_t sphase = 0, ephase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       const int nch = (it.n + 3) >> 2;  // 4-token chunks with real tokens
@@ -539,7 +527,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       bool ok = true;
       for (int kb = 0; kb < a.S; ++kb) {
         if (!GD_WAIT(&tl.sc_full[sslot], sphase, abort_flag, a.status) ||
-            !GD_WAIT(&tl.ps_full[ps], pphase, abort_flag, a.status)) {
+            !GD_WAIT(&tl.empty[eslot], ephase, abort_flag, a.status)) {  // this stage's MMAs
           ok = false;
           break;
         }
@@ -570,7 +558,8 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl.ps_empty[ps]);
         if (++sslot == C::NSS) { sslot = 0; sphase ^= 1u; }
-        if (++ps == C::NPS) { ps = 0; pphase ^= 1u; }
+        if (++eslot == C::NS) { eslot = 0; ephase ^= 1u; }
+        if (++ps == C::NPS) ps = 0;
       }
       if (!ok) break;
       // ---- item result: h = silu(gate) * up (one output tile), or y (two); row r of each

@@ -119,6 +119,21 @@ def recorded_traffic(kernel: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(pg, v: float, dev) -> float:
+    """The largest of every rank's v (the job's time is its slowest replica's)."""
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest replica's time."""
+    return T * steps * world / (max_ms / 1e3)
+
+
 def unique_experts(ids: np.ndarray) -> int:
     return int(len(np.unique(ids)))
 
@@ -230,10 +245,9 @@ def main():
     U = head["U"]
     T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
     P = T * k
-    tokens_all = T * args.steps * world
-    value = tokens_all / (head["max_ms"] / 1e3)
+    value = job_tokens_per_s(T, args.steps, world, head["max_ms"])
     roofline = ffn_roofline(L, U, head["ffn_ms"], pk, pk_kind, cfg["workload"], args.ffn_path)
-    e2e_val = tokens_all / (head["e2e_max_ms"] / 1e3)
+    e2e_val = job_tokens_per_s(T, args.steps, world, head["e2e_max_ms"])
 
     # ---- decode sweep over the other batch sizes (informative)
     sweep = {}
@@ -504,12 +518,7 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
         step_ms = timed(graph.replay, steps)
     if pg:
         pg.barrier()
-    my_ms = float(np.sum(step_ms))
-    max_ms = my_ms
-    if pg:
-        t = torch.tensor([my_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(pg, float(np.sum(step_ms)), dev)
 
     # the expert FFN alone (its two launches), inputs from this routing
     ws_n = F.ftmoe_ffn_workspace_bytes(T, k, E, H, I)
@@ -552,13 +561,7 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
         for _ in range(3):
             e2e_graph.replay()
         torch.cuda.synchronize()
-        e2e_ms = float(np.sum(timed(e2e_graph.replay, steps)))
-        e2e_max = e2e_ms
-        if pg:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_max = float(t.item())
-        res["e2e_max_ms"] = e2e_max
+        res["e2e_max_ms"] = max_over_ranks(pg, float(np.sum(timed(e2e_graph.replay, steps))), dev)
     return res
 
 

@@ -34,3 +34,4 @@ from .permute import permute  # noqa: F401
 from .ffn import combine, expert_ffn, silu, swiglu_ffn  # noqa: F401
 from .layer import layer, layer_rows  # noqa: F401
 from .cache import LRUSim  # noqa: F401
+from .gate import gate  # noqa: F401

@@ -11,6 +11,7 @@ from .gen import (  # noqa: F401
     QTYPE_BLOCK_BYTES,
     bf16_bits_to_f32,
     f32_to_bf16_bits,
+    gen_gate_weights,
     gen_logits,
     gen_x_bf16,
     gen_expert_weights,

@@ -66,6 +66,13 @@ def gen_x_bf16(seed: int, T: int, H: int, tag: str = "x") -> np.ndarray:
     return f32_to_bf16_bits(x)
 
 
+def gen_gate_weights(seed: int, E: int, H: int, tag: str = "gate") -> np.ndarray:
+    """Router gate matrix ~N(0, 1/H) rounded to bf16 (logits of unit scale for unit
+    activations); uint16 bits [E, H]."""
+    w = _rng(seed, tag, E, H).standard_normal((E, H), dtype=np.float32) / np.float32(np.sqrt(H))
+    return f32_to_bf16_bits(w)
+
+
 def zipf_bias(E: int, s: float) -> np.ndarray:
     """Expert popularity skew added to router logits: -s * ln(e + 1) (expert 0 most popular)."""
     return -s * np.log(np.arange(1, E + 1, dtype=np.float64))

@@ -199,6 +199,7 @@ def main():
                     help="skip the extra prefill-layer measurement of the default run")
     ap.add_argument("--ffn-path", default="auto", choices=list(FFN_PATHS),
                     help="expert-FFN kernel (auto: GEMM at >= 32 rows per expert, else GEMV)")
+    ap.add_argument("--no-gate", action="store_true", help="skip the router-gate measurement")
     ap.add_argument("--stream-steps", type=int, default=256,
                     help="timed decode steps of the 48-layer expert-cache stream (0: skip)")
     args = ap.parse_args()
@@ -279,6 +280,12 @@ def main():
                            "roofline": ffn_roofline(Lp, r["U"], r["ffn_ms"], pk, pk_kind, wl)}
         F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
 
+    # ---- the router gate ahead of the layer (hidden state -> logits), decode and prefill sizes
+    gate = None
+    if args.config == "decode" and not args.no_gate:
+        gate = {f"T{Tg}": measure_gate(dev, Tg, H, E, flush, stream, pk, pk_kind, max(10, args.steps // 4))
+                for Tg in (T, CONFIGS["prefill"]["T"])}
+
     # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
     stream_res = None
     if args.stream_steps > 0 and args.config == "decode":
@@ -312,10 +319,39 @@ def main():
             "decode_sweep": sweep or None,
             "prefill": prefill,
             "stream": stream_res,
+            "gate": gate,
         }
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def measure_gate(dev, T, H, E, flush, stream, pk, pk_kind, reps):
+    """ftmoe_gate (hidden state -> expert logits) on seeded inputs, L2 flushed between
+    launches; algorithmic bytes = the gate matrix + the hidden rows + the logits."""
+    import torch
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    from synth import gen_gate_weights, gen_x_bf16
+    x = torch.from_numpy(gen_x_bf16(31, T, H, "gate_x").view(np.int16)).to(dev).view(torch.bfloat16)
+    wg = torch.from_numpy(gen_gate_weights(32, E, H).view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, E), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        F.ftmoe_gate(x, wg, T, H, E, out)
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        F.ftmoe_gate(x, wg, T, H, E, out)
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    alg = E * H * 2 + T * H * 2 + T * E * 4
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": f"gate T{T} H{H} E{E} bf16 -> fp32", "us_per_launch": ms * 1e3,
+            "alg_bytes": alg, "achieved_gbs": gbs, "hbm_frac": gbs / float(pk["hbm_gbs"]),
+            "tflops": 2.0 * T * H * E / (ms / 1e3) / 1e12, "peak_kind": f"{pk_kind} hbm_gbs"}
 
 
 def host_mem_available() -> int:

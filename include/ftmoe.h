@@ -116,6 +116,19 @@ ftmoe_status ftmoe_repack(int qtype, const void* canon, void* tiles, int E, int 
 ftmoe_status ftmoe_dequant(int qtype, const void* tiles, int E, int N, int K, float* out,
                            ftmoe_stream_t stream);
 
+/* ------------------------------------------------------------------ gate
+ * The scores the router selects from ([P3] sparse expert activation), from the
+ * hidden state: logits[t][e] = sum over h of x[t][h] * wg[e][h].
+ *   x:      device bf16 [T][H];  wg: device bf16 [E][H] (gate matrix, one row per
+ *           expert, the reduction dimension last);
+ *   logits: device fp32 [T][E] (out).
+ * fp32 accumulation in a fixed order that depends only on H (16-element steps
+ * taken by 16 interleaved slices, the slices added in order), so a token's logits
+ * do not depend on the batch.  H a multiple of 32 up to 16384, 1 <= E <= 1024;
+ * T == 0 is a no-op.  Not part of ftmoe_layer, which starts from logits. */
+ftmoe_status ftmoe_gate(const uint16_t* x, const uint16_t* wg, int T, int H, int E, float* logits,
+                        ftmoe_stream_t stream);
+
 /* ------------------------------------------------------------------ route
  * Per token t ([P3] sparse expert activation): ids[t][0..k) = the k experts
  * with the largest logits[t][:], in descending logit order, ties to the lower

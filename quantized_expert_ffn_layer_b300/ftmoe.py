@@ -77,6 +77,7 @@ _SIGS = {
     "ftmoe_layer": (_i, [C.POINTER(ftmoe_weights), _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ftmoe_device_status": (_i, [C.POINTER(_i), _vp]),
     "ftmoe_check_wait_timeout": (_i, [C.c_longlong, _vp, _vp]),
+    "ftmoe_gate": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "ftmoe_cache_create": (_i, [C.POINTER(ftmoe_cache_desc), C.POINTER(_vp)]),
     "ftmoe_cache_prefetch": (_i, [_vp, _i, _vp, _i, _vp, _vp]),
     "ftmoe_cache_acquire": (_i, [_vp, _i, _vp, _i, _vp, C.POINTER(_vp), _vp, _vp]),
@@ -202,6 +203,10 @@ def ftmoe_device_status(stream=None):
     code = C.c_int(0)
     _check("ftmoe_device_status", lib.ftmoe_device_status(C.byref(code), _s(stream)))
     return code.value
+
+
+def ftmoe_gate(x, wg, T, H, E, logits, stream=None):
+    _check("ftmoe_gate", lib.ftmoe_gate(_p(x), _p(wg), T, H, E, _p(logits), _s(stream)))
 
 
 def ftmoe_check_wait_timeout(limit_ns, waited_ok=None, stream=None):

@@ -49,4 +49,12 @@ def test_invalid_arguments_rejected_on_host(F):
     # T == 0 is a successful no-op for route
     F.ftmoe_route(0, 0, 8, 2, 0, 0, stream=0)
     assert F.ftmoe_status_string(4) if hasattr(F, "ftmoe_status_string") else True
-    assert F.ftmoe_set_ffn_path(0) in (0, 1, 2)
+    assert F.ftmoe_set_ffn_path(0) in (0, 1, 2, 3)
+    # gate: H must be a multiple of 32, E in [1, 1024]; T == 0 is a no-op
+    for T, H, E in ((4, 48, 8), (4, 64, 0), (4, 64, 1025), (-1, 64, 8)):
+        with pytest.raises(F.FtmoeError) as ei:
+            F.ftmoe_gate(1, 1, T, H, E, 1, stream=0)
+        assert ei.value.status == 1
+    with pytest.raises(F.FtmoeError):
+        F.ftmoe_gate(0, 0, 4, 64, 8, 0, stream=0)  # null pointers
+    F.ftmoe_gate(0, 0, 0, 64, 8, 0, stream=0)

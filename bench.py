@@ -200,6 +200,8 @@ def main():
     ap.add_argument("--ffn-path", default="auto", choices=list(FFN_PATHS),
                     help="expert-FFN kernel (auto: GEMM at >= 32 rows per expert, else GEMV)")
     ap.add_argument("--no-gate", action="store_true", help="skip the router-gate measurement")
+    ap.add_argument("--prefill-stream-chunks", type=int, default=2,
+                    help="timed prefill chunks through the streamed 48-layer bank (0: skip)")
     ap.add_argument("--stream-steps", type=int, default=256,
                     help="timed decode steps of the 48-layer expert-cache stream (0: skip)")
     args = ap.parse_args()
@@ -287,9 +289,16 @@ def main():
                 for Tg in (T, CONFIGS["prefill"]["T"])}
 
     # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
-    stream_res = None
-    if args.stream_steps > 0 and args.config == "decode":
-        stream_res = measure_stream(L, dev, args.stream_steps, 16, rank)
+    stream_res = pstream = None
+    if args.config == "decode" and (args.stream_steps > 0 or args.prefill_stream_chunks > 0):
+        ctx = stream_bank(L, dev)
+        if args.stream_steps > 0:
+            stream_res = measure_stream(L, dev, args.stream_steps, 16, rank, ctx)
+        if args.prefill_stream_chunks > 0:
+            F.ftmoe_set_ffn_path(FFN_PATHS["auto"])
+            pstream = measure_prefill_stream(dev, args.prefill_stream_chunks, ctx)
+            F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
+        del ctx
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -319,6 +328,7 @@ def main():
             "decode_sweep": sweep or None,
             "prefill": prefill,
             "stream": stream_res,
+            "prefill_stream": pstream,
             "gate": gate,
         }
         print(json.dumps(line), flush=True)
@@ -365,7 +375,54 @@ def host_mem_available() -> int:
     return 0
 
 
-def measure_stream(L, dev, steps, warmup, rank):
+def stream_bank(L, dev):
+    """The 48-layer pinned-host expert bank of the stream workload (every layer holds the
+    decode layer's expert blobs: only the bytes' path matters) and the pinned-copy peak."""
+    import torch
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    E, H, I = L.E, L.H, L.I
+    m = MoELayer(L.qtype, E, H, I, L.w13, L.w2, device=dev)
+    nb = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
+    layers = CONFIGS["stream"]["layers"]
+    # the bank is pinned host memory: keep it within half of what the host has free
+    avail = host_mem_available()
+    if avail and layers * E * nb > avail // 2:
+        layers = max(2, int(avail // 2 // (E * nb)))
+    blobs = torch.cat([m.w13.view(E, -1), m.w2.view(E, -1)], dim=1).cpu()
+    assert blobs.shape[1] == nb
+    bank = torch.empty((layers, E, nb), dtype=torch.uint8, pin_memory=True)
+    for l in range(layers):
+        bank[l].copy_(blobs)
+    # plain pinned host -> device copy bandwidth (the PCIe ceiling for the copies)
+    src = bank.view(-1)[: 1 << 30]
+    dst = torch.empty(src.numel(), dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(4):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    pcie_gbs = 4 * src.numel() / (a.elapsed_time(b) / 1e3) / 1e9
+    del dst
+    return {"m": m, "bank": bank, "layers": layers, "nb": nb, "pinned_copy_gbs": pcie_gbs}
+
+
+def _timed_region(fn, stream):
+    import torch
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b), (time.perf_counter() - t0) * 1e3
+
+
+def measure_stream(L, dev, steps, warmup, rank, ctx):
     """Batch-1 decode through a stack of layers whose expert weights live in a pinned-host
     bank and are streamed into a per-layer LRU slot pool (25% of the experts).  Per layer:
     prefetch the next layer's experts on the copy stream, acquire this layer's (the compute
@@ -373,24 +430,12 @@ def measure_stream(L, dev, steps, warmup, rank):
     Reports tokens/s, the hit rate, the achieved host->device bandwidth against a plain
     pinned copy, and the same layers with every expert resident (no cache) for the bound."""
     import torch
-    from quantized_expert_ffn_layer_b300 import MoELayer
     from quantized_expert_ffn_layer_b300 import ftmoe as F
     from synth import stream_trace
     c = CONFIGS["stream"]
     E, k, H, I = L.E, L.k, L.H, L.I
-    m = MoELayer(L.qtype, E, H, I, L.w13, L.w2, device=dev)
-    nb = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
-    layers = c["layers"]
-    # the bank is pinned host memory: keep it within half of what the host has free
-    avail = host_mem_available()
-    if avail and layers * E * nb > avail // 2:
-        layers = max(2, int(avail // 2 // (E * nb)))
+    m, bank, layers, nb = ctx["m"], ctx["bank"], ctx["layers"], ctx["nb"]
     slots = c["slots"]
-    blobs = torch.cat([m.w13.view(E, -1), m.w2.view(E, -1)], dim=1).cpu()
-    assert blobs.shape[1] == nb
-    bank = torch.empty((layers, E, nb), dtype=torch.uint8, pin_memory=True)
-    for l in range(layers):
-        bank[l].copy_(blobs)  # every layer holds the same expert draws; only the bytes' path matters
     pool = torch.empty(layers * slots * nb, dtype=torch.uint8, device=dev)
     copy_stream = torch.cuda.Stream(dev)
     compute = torch.cuda.current_stream(dev)
@@ -409,25 +454,42 @@ def measure_stream(L, dev, steps, warmup, rank):
     wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))  # filled by every acquire
     ids_py = trace.tolist()
 
-    def run_steps(s0, s1):
+    def run_steps(s0, s1, mode="known"):
+        """known: layer l+1's ids are known when layer l starts and are prefetched then;
+        history: layer l+1's ids of its previous acquire are prefetched instead (the true
+        ids are only known at the acquire); on_demand: no prefetch at all."""
         for st in range(s0, s1):
-            cache.prefetch(0, ids_py[st][0])
+            if mode == "known":
+                cache.prefetch(0, ids_py[st][0])
             for l in range(layers):
-                if l + 1 < layers:
+                if mode == "known" and l + 1 < layers:
                     cache.prefetch(l + 1, ids_py[st][l + 1])
+                elif mode == "history":
+                    cache.prefetch_history((l + 1) % layers)
                 cache.acquire(l, ids_py[st][l], compute)
                 F.ftmoe_layer(wts, lg_d[st, l:l + 1], x, 1, k, out, None, None, ws, ws.numel())
                 cache.release(l, compute)
 
     def timed(fn):
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        a.record(compute)
-        fn()
-        b.record(compute)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b), (time.perf_counter() - t0) * 1e3
+        return _timed_region(fn, compute)
+
+    # the two modes without the layer's ids ahead of time, each on a fresh cache
+    modes = {}
+    for mode in ("history", "on_demand"):
+        cm = F.ExpertCache(layers, E, nb, bank, pool, slots, F.LRU_PER_LAYER, copy_stream)
+        cache, keep = cm, cache
+        wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))
+        run_steps(0, warmup, mode)
+        a0 = cache.stats()
+        mms, _ = timed(lambda: run_steps(warmup, total, mode))
+        a1 = cache.stats()
+        dd = {f: a1[f] - a0[f] for f in a1}
+        modes[mode] = {"tokens_per_s": steps / (mms / 1e3), "ms_per_token": mms / steps,
+                       "hit_rate": dd["hits"] / max(1, dd["lookups"]),
+                       "h2d_bytes_per_token": dd["h2d_bytes"] / steps}
+        cache.close()
+        cache = keep
+        wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))
 
     run_steps(0, warmup)
     s0 = cache.stats()
@@ -440,12 +502,7 @@ def measure_stream(L, dev, steps, warmup, rank):
             for l in range(layers):
                 F.ftmoe_layer(m.weights, lg_d[st, l:l + 1], x, 1, k, out, None, None, ws, ws.numel())
     res_ms, res_wall = timed(resident)
-    # plain pinned host -> device copy bandwidth (the PCIe ceiling for the misses)
-    src = bank.view(-1)[: 1 << 30]
-    dst = torch.empty(src.numel(), dtype=torch.uint8, device=dev)
-    dst.copy_(src, non_blocking=True)
-    cp_ms, _ = timed(lambda: [dst.copy_(src, non_blocking=True) for _ in range(4)])
-    pcie_gbs = 4 * src.numel() / (cp_ms / 1e3) / 1e9
+    pcie_gbs = ctx["pinned_copy_gbs"]
     h2d_gbs = d["h2d_bytes"] / (ms / 1e3) / 1e9
     bound_ms = max(res_ms, d["h2d_bytes"] / (pcie_gbs * 1e9) * 1e3)
     cache.close()
@@ -459,10 +516,74 @@ def measure_stream(L, dev, steps, warmup, rank):
              "h2d_bytes_per_token": d["h2d_bytes"] / steps, "h2d_gbs": h2d_gbs,
              "pinned_copy_gbs": pcie_gbs, "h2d_frac": h2d_gbs / pcie_gbs,
              "resident_ms_per_token": res_ms / steps,
-             "bound_ms_per_token": bound_ms / steps, "frac_of_bound": bound_ms / ms}
-    del bank, pool, dst
+             "bound_ms_per_token": bound_ms / steps, "frac_of_bound": bound_ms / ms,
+             "ids_ahead": "known one layer ahead (the numbers above)",
+             "without_ids_ahead": modes}
+    del pool
     torch.cuda.empty_cache()
     return out_d
+
+
+def measure_prefill_stream(dev, chunks, ctx):
+    """Chunked prefill through the stack of layers with the whole bank streamed: a global
+    LRU pool a little over two layers deep, every layer's experts acquired, the next
+    layer's all prefetched on the copy stream while this layer's chunk computes (full-layer
+    double buffering).  Reports tokens/s, the copy bandwidth against a plain pinned copy,
+    the same chunks with every expert resident, and the overlap efficiency
+    (t_copy + t_compute - t_measured) / min(t_copy, t_compute): 1 = fully hidden."""
+    import ctypes as C
+    import torch
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    from synth import gen_logits, gen_x_bf16
+    m, bank, layers, nb = ctx["m"], ctx["bank"], ctx["layers"], ctx["nb"]
+    E, H, I = m.E, m.H, m.I
+    cp = CONFIGS["prefill"]
+    T, k = cp["T"], cp["k"]
+    per_layer = -(-2 * E // layers)  # global pool of >= 2 E slots
+    pool = torch.empty(layers * per_layer * nb, dtype=torch.uint8, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    compute = torch.cuda.current_stream(dev)
+    cache = F.ExpertCache(layers, E, nb, bank, pool, per_layer, F.LRU_GLOBAL, copy_stream)
+    x = torch.from_numpy(gen_x_bf16(41, T, H, "pstream_x").view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(gen_logits(42, T, E, zipf=cp["zipf"], tag="pstream_logits")).to(dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = m.workspace(T, k)
+    wts = F.make_weights(m.qtype, E, H, I)
+    wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))
+    everyone = list(range(E))
+
+    def run(n):
+        for _ in range(n):
+            for l in range(layers):
+                cache.acquire(l, everyone, compute)
+                cache.prefetch((l + 1) % layers, everyone)
+                F.ftmoe_layer(wts, lg, x, T, k, out, None, None, ws, ws.numel())
+                cache.release(l, compute)
+
+    def resident(n):
+        for _ in range(n):
+            for l in range(layers):
+                F.ftmoe_layer(m.weights, lg, x, T, k, out, None, None, ws, ws.numel())
+
+    run(1)
+    s0 = cache.stats()
+    ms, _ = _timed_region(lambda: run(chunks), compute)
+    s1 = cache.stats()
+    res_ms, _ = _timed_region(lambda: resident(chunks), compute)
+    cache.close()
+    h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
+    t_copy = h2d / (ctx["pinned_copy_gbs"] * 1e9) * 1e3
+    overlap = (t_copy + res_ms - ms) / min(t_copy, res_ms)
+    del pool
+    torch.cuda.empty_cache()
+    return {"workload": f"chunked prefill, {layers} layers H{H} I{I} E{E} top-{k} {m.qtype}, "
+                        f"{T}-token chunks, whole layers streamed (global LRU, {layers * per_layer} slots)",
+            "chunks": chunks, "tokens_per_s": T * chunks / (ms / 1e3), "ms_per_layer": ms / (chunks * layers),
+            "h2d_bytes_per_layer": h2d / (chunks * layers), "h2d_gbs": h2d / (ms / 1e3) / 1e9,
+            "pinned_copy_gbs": ctx["pinned_copy_gbs"],
+            "h2d_frac": h2d / (ms / 1e3) / 1e9 / ctx["pinned_copy_gbs"],
+            "resident_ms_per_layer": res_ms / (chunks * layers),
+            "copy_ms_per_layer_at_peak": t_copy / (chunks * layers), "overlap_efficiency": overlap}
 
 
 def ffn_path_used(P, E, path):

@@ -293,6 +293,16 @@ ftmoe_status ftmoe_cache_create(const ftmoe_cache_desc* desc, ftmoe_cache** out)
 ftmoe_status ftmoe_cache_prefetch(ftmoe_cache* c, int layer, const int32_t* ids, int n,
                                   int32_t* slots_out, uint8_t* copied_out);
 
+/* Predictive prefetch from routing history ([P4] 方法: the decode phase predicts
+ * the experts it needs; 核心洞察: consecutive agent steps reuse experts), in its
+ * plainest form: ftmoe_cache_prefetch of the ids that `layer`'s most recent
+ * ftmoe_cache_acquire asked for, in that order.  ids_out (host int32 [E],
+ * nullable) receives those ids and *n_out their count (0, and nothing issued,
+ * when the layer has not been acquired yet); slots_out / copied_out (host,
+ * nullable, at least E entries) as for prefetch. */
+ftmoe_status ftmoe_cache_prefetch_history(ftmoe_cache* c, int layer, int32_t* ids_out, int* n_out,
+                                          int32_t* slots_out, uint8_t* copied_out);
+
 /* Make `layer`'s experts ids[0..n) resident (copying misses) and make `compute`
  * wait for their copies.  blob_out: host array of E pointers, filled for the
  * requested ids (other entries untouched), ready for ftmoe_weights.expert_blob.

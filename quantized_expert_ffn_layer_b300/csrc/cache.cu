@@ -21,7 +21,8 @@ struct ftmoe_cache {
   std::vector<cudaEvent_t> copy_done, busy;
   std::vector<char> copy_unwaited, has_busy;
   std::unordered_map<long long, int> where;   // (layer * E + e) -> global slot
-  std::vector<std::vector<int>> last_acquired;  // per layer
+  std::vector<std::vector<int>> last_acquired;  // per layer: global slots of the last acquire
+  std::vector<std::vector<int32_t>> last_ids;   // per layer: expert ids of the last acquire
   std::vector<cudaEvent_t> layer_done;          // per layer, recorded at release
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timing_pending;
   std::vector<cudaEvent_t> timing_free;
@@ -146,6 +147,7 @@ ftmoe_status ftmoe_cache_create(const ftmoe_cache_desc* d, ftmoe_cache** out) {
   c->copy_unwaited.assign(total, 0);
   c->has_busy.assign(total, 0);
   c->last_acquired.resize(d->layers);
+  c->last_ids.resize(d->layers);
   c->layer_done.assign(d->layers, nullptr);
   bool ok = true;
   for (int i = 0; i < total && ok; ++i)
@@ -194,7 +196,22 @@ ftmoe_status ftmoe_cache_acquire(ftmoe_cache* c, int layer, const int32_t* ids, 
     blob_out[ids[i]] = (const char*)c->d.pool + (size_t)g * c->d.blob_bytes;
   }
   c->last_acquired[layer] = gs;
+  c->last_ids[layer].assign(ids, ids + n);
   return FTMOE_OK;
+}
+
+// Semantic-aware expert caching (the edge-serving digest, 方法: the decode phase
+// predicts the experts it will need to raise the hit rate; 核心洞察: consecutive agent
+// steps reuse experts) in its plainest form: predict that a layer needs what it needed
+// at its last acquire.
+ftmoe_status ftmoe_cache_prefetch_history(ftmoe_cache* c, int layer, int32_t* ids_out, int* n_out,
+                                          int32_t* slots_out, uint8_t* copied_out) {
+  if (!c || !n_out || layer < 0 || layer >= c->d.layers) return FTMOE_ERR_INVALID_ARG;
+  const std::vector<int32_t> ids = c->last_ids[layer];  // (request() may not change it, but copy)
+  *n_out = (int)ids.size();
+  if (ids_out && !ids.empty()) std::memcpy(ids_out, ids.data(), ids.size() * sizeof(int32_t));
+  if (ids.empty()) return FTMOE_OK;
+  return ftmoe_cache_prefetch(c, layer, ids.data(), (int)ids.size(), slots_out, copied_out);
 }
 
 ftmoe_status ftmoe_cache_release(ftmoe_cache* c, int layer, ftmoe_stream_t compute) {

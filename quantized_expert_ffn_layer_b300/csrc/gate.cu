@@ -15,6 +15,7 @@ namespace ftmoe {
 constexpr int GT_TOK = 16;
 constexpr int GT_EXP = 32;
 constexpr int GT_WARPS = 16;
+constexpr int GT_U = 4;  // k-steps per load round
 
 __device__ __forceinline__ uint32_t ld32_or0(const uint16_t* row, int h) {
   return row ? __ldg(reinterpret_cast<const uint32_t*>(row + h)) : 0u;
@@ -37,11 +38,30 @@ __global__ void __launch_bounds__(GT_WARPS * 32) gate_kernel(const uint16_t* __r
     wr[j] = e < E ? wg + (size_t)e * H : nullptr;
   }
   float acc[4][4] = {};
-  for (int k0 = 16 * w; k0 < H; k0 += 16 * GT_WARPS) {
-    const int h0 = k0 + 2 * c, h1 = h0 + 8;
-    const uint32_t a[4] = {ld32_or0(xa, h0), ld32_or0(xb, h0), ld32_or0(xa, h1), ld32_or0(xb, h1)};
+  // GT_U of the warp's k-steps per round: every load of the round is issued before the
+  // first MMA, so a round costs one memory latency; the MMAs still run in k order.
+  constexpr int STEP = 16 * GT_WARPS;
+  for (int k0 = 16 * w; k0 < H; k0 += GT_U * STEP) {
+    uint32_t a[GT_U][4], b[GT_U][4][2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mma_16816(acc[j], a, ld32_or0(wr[j], h0), ld32_or0(wr[j], h1));
+    for (int u = 0; u < GT_U; ++u) {
+      const bool in = k0 + u * STEP < H;
+      const int h0 = k0 + u * STEP + 2 * c, h1 = h0 + 8;
+      a[u][0] = in ? ld32_or0(xa, h0) : 0u;
+      a[u][1] = in ? ld32_or0(xb, h0) : 0u;
+      a[u][2] = in ? ld32_or0(xa, h1) : 0u;
+      a[u][3] = in ? ld32_or0(xb, h1) : 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        b[u][j][0] = in ? ld32_or0(wr[j], h0) : 0u;
+        b[u][j][1] = in ? ld32_or0(wr[j], h1) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < GT_U; ++u)
+      if (k0 + u * STEP < H)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_16816(acc[j], a[u], b[u][j][0], b[u][j][1]);
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {

@@ -81,6 +81,7 @@ _SIGS = {
     "ftmoe_cache_create": (_i, [C.POINTER(ftmoe_cache_desc), C.POINTER(_vp)]),
     "ftmoe_cache_prefetch": (_i, [_vp, _i, _vp, _i, _vp, _vp]),
     "ftmoe_cache_acquire": (_i, [_vp, _i, _vp, _i, _vp, C.POINTER(_vp), _vp, _vp]),
+    "ftmoe_cache_prefetch_history": (_i, [_vp, _i, _vp, C.POINTER(_i), _vp, _vp]),
     "ftmoe_cache_release": (_i, [_vp, _i, _vp]),
     "ftmoe_cache_stats_get": (_i, [_vp, C.POINTER(ftmoe_cache_stats)]),
     "ftmoe_cache_destroy": (_i, [_vp]),
@@ -238,6 +239,17 @@ class ExpertCache:
         copied = (C.c_uint8 * len(ids))()
         _check("ftmoe_cache_prefetch", lib.ftmoe_cache_prefetch(self.h, layer, a, len(ids), slots, copied))
         return list(slots), [bool(c) for c in copied]
+
+    def prefetch_history(self, layer):
+        """Prefetch what `layer` asked for at its last acquire; returns (ids, slots, copied)."""
+        ids = (C.c_int32 * self.E)()
+        slots = (C.c_int32 * self.E)()
+        copied = (C.c_uint8 * self.E)()
+        n = C.c_int(0)
+        _check("ftmoe_cache_prefetch_history",
+               lib.ftmoe_cache_prefetch_history(self.h, layer, ids, C.byref(n), slots, copied))
+        k = n.value
+        return list(ids)[:k], list(slots)[:k], [bool(c) for c in list(copied)[:k]]
 
     def acquire(self, layer, ids, compute_stream=None):
         a = self._ids(ids)

@@ -113,3 +113,40 @@ def test_cache_rejects_requests_larger_than_the_pool(env):
         cache.prefetch(0, [0, E])  # expert id out of range
     assert ei.value.status == 1
     cache.close()
+
+
+@pytest.mark.parametrize("policy", ["layer", "global"])
+def test_history_prefetch_matches_simulator(env, policy):
+    """Predictive prefetch from routing history: at each layer, prefetch what the next
+    layer asked for at its previous acquire, then acquire this layer's true ids.  Every
+    slot choice, hit and miss must equal the LRU simulator driven by the same requests."""
+    F, torch, dev = env
+    layers, bank, nb = _bank(env, "q4_0")
+    pool = torch.zeros(LAYERS * SLOTS * nb, dtype=torch.uint8, device=dev)
+    pol = F.LRU_PER_LAYER if policy == "layer" else F.LRU_GLOBAL
+    cache = F.ExpertCache(LAYERS, E, nb, bank, pool, SLOTS, pol, torch.cuda.Stream(dev))
+    sim = oracle.LRUSim(LAYERS, E, SLOTS, policy)
+    compute = torch.cuda.current_stream(dev)
+    steps = 10
+    trace = stream_trace(9, steps, LAYERS, E, K, p_repeat=0.6, s=1.0)
+    last = {}
+    for st in range(steps):
+        for l in range(LAYERS):
+            nxt = (l + 1) % LAYERS
+            ids, slots, copied = cache.prefetch_history(nxt)
+            assert ids == last.get(nxt, [])
+            if ids:
+                want = sim.request(nxt, ids)
+                assert [s for s, _ in want] == slots and [c for _, c in want] == copied
+            _, slots, copied = cache.acquire(l, trace[st, l], compute)
+            want = sim.request(l, trace[st, l])
+            assert [s for s, _ in want] == slots and [c for _, c in want] == copied
+            last[l] = [int(v) for v in trace[st, l]]
+            cache.release(l, compute)
+    torch.cuda.synchronize()
+    pool_h = pool.view(-1, nb).cpu()
+    nslot = SLOTS if policy == "layer" else SLOTS * LAYERS
+    for (l, e), s in sim.where.items():
+        gs = (l * nslot + s) if policy == "layer" else s
+        assert torch.equal(pool_h[gs], bank[l, e]), (l, e, s)
+    cache.close()

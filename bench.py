@@ -456,19 +456,23 @@ def measure_stream(L, dev, steps, warmup, rank, ctx):
 
     def run_steps(s0, s1, mode="known"):
         """known: layer l+1's ids are known when layer l starts and are prefetched then;
-        history: layer l+1's ids of its previous acquire are prefetched instead (the true
-        ids are only known at the acquire); on_demand: no prefetch at all."""
+        on_demand: a layer's ids are known only once the layer before it has run (the host
+        waits for it, as it would to read the routing), so its misses are copied then;
+        history: as on_demand, but while layer l runs the copy stream already fetches what
+        layer l+1 asked for at its previous acquire."""
         for st in range(s0, s1):
             if mode == "known":
                 cache.prefetch(0, ids_py[st][0])
             for l in range(layers):
                 if mode == "known" and l + 1 < layers:
                     cache.prefetch(l + 1, ids_py[st][l + 1])
-                elif mode == "history":
-                    cache.prefetch_history((l + 1) % layers)
+                if mode != "known":
+                    compute.synchronize()  # the previous layer's routing is known now
                 cache.acquire(l, ids_py[st][l], compute)
                 F.ftmoe_layer(wts, lg_d[st, l:l + 1], x, 1, k, out, None, None, ws, ws.numel())
                 cache.release(l, compute)
+                if mode == "history":
+                    cache.prefetch_history((l + 1) % layers)
 
     def timed(fn):
         return _timed_region(fn, compute)
@@ -486,7 +490,8 @@ def measure_stream(L, dev, steps, warmup, rank, ctx):
         dd = {f: a1[f] - a0[f] for f in a1}
         modes[mode] = {"tokens_per_s": steps / (mms / 1e3), "ms_per_token": mms / steps,
                        "hit_rate": dd["hits"] / max(1, dd["lookups"]),
-                       "h2d_bytes_per_token": dd["h2d_bytes"] / steps}
+                       "h2d_bytes_per_token": dd["h2d_bytes"] / steps,
+                       "prefetch_copies_per_token": dd["prefetch_copies"] / steps}
         cache.close()
         cache = keep
         wts.expert_blob = C.cast(cache._blob, C.POINTER(C.c_void_p))
@@ -530,7 +535,8 @@ def measure_prefill_stream(dev, chunks, ctx):
     layer's all prefetched on the copy stream while this layer's chunk computes (full-layer
     double buffering).  Reports tokens/s, the copy bandwidth against a plain pinned copy,
     the same chunks with every expert resident, and the overlap efficiency
-    (t_copy + t_compute - t_measured) / min(t_copy, t_compute): 1 = fully hidden."""
+    (t_copy + t_compute - t_measured) / min(t_copy, t_compute) with t_copy the copies'
+    own measured durations: 1 = the shorter of the two fully hidden."""
     import ctypes as C
     import torch
     from quantized_expert_ffn_layer_b300 import ftmoe as F
@@ -572,7 +578,7 @@ def measure_prefill_stream(dev, chunks, ctx):
     res_ms, _ = _timed_region(lambda: resident(chunks), compute)
     cache.close()
     h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
-    t_copy = h2d / (ctx["pinned_copy_gbs"] * 1e9) * 1e3
+    t_copy = s1["h2d_ms"] - s0["h2d_ms"]  # the copies' own durations (events on the copy stream)
     overlap = (t_copy + res_ms - ms) / min(t_copy, res_ms)
     del pool
     torch.cuda.empty_cache()
@@ -583,7 +589,7 @@ def measure_prefill_stream(dev, chunks, ctx):
             "pinned_copy_gbs": ctx["pinned_copy_gbs"],
             "h2d_frac": h2d / (ms / 1e3) / 1e9 / ctx["pinned_copy_gbs"],
             "resident_ms_per_layer": res_ms / (chunks * layers),
-            "copy_ms_per_layer_at_peak": t_copy / (chunks * layers), "overlap_efficiency": overlap}
+            "copy_ms_per_layer": t_copy / (chunks * layers), "overlap_efficiency": overlap}
 
 
 def ffn_path_used(P, E, path):

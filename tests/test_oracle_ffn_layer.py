@@ -78,3 +78,29 @@ def test_per_token_definition_matches_grouped_and_shared_expert_adds():
     assert np.allclose(out, r["out"][rows], rtol=1e-12, atol=1e-15)
     r0 = layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2)
     assert np.allclose(r["out"] - r0["out"], r["shared_y"], rtol=1e-10, atol=1e-14)
+
+
+def test_silu_identities():
+    """silu(x) = x * sigmoid(x) pinned by facts that do not retype it: silu(x) - silu(-x)
+    = x (sigmoid(x) + sigmoid(-x) = 1), silu(0) = 0, the tanh form of the sigmoid, and
+    the limits x (x -> +inf) and 0 (x -> -inf)."""
+    from oracle import silu
+    x = np.linspace(-30.0, 30.0, 1201)
+    assert np.allclose(silu(x) - silu(-x), x, rtol=0, atol=1e-12)
+    assert silu(np.array([0.0]))[0] == 0.0
+    xm = np.linspace(-8.0, 8.0, 321)  # (1 + tanh) cancels for large negative x
+    assert np.allclose(silu(xm), xm * 0.5 * (1.0 + np.tanh(0.5 * xm)), rtol=1e-12, atol=1e-15)
+    assert abs(silu(np.array([60.0]))[0] - 60.0) < 1e-20 and abs(silu(np.array([-60.0]))[0]) < 1e-24
+
+
+def test_gate_rows_come_first_and_up_multiplies():
+    """w13 holds the gate rows first: with gate rows giving 2 and up rows giving 3 the
+    hidden value is silu(2) * 3, not silu(3) * 2 (a swapped half would give the latter)."""
+    H, I = 4, 2
+    X = np.ones((1, H))
+    W13 = np.vstack([np.full((I, H), 0.5), np.full((I, H), 0.75)])  # gate 2, up 3
+    W2 = np.eye(H, I)  # y[o] = h[o] for o < I
+    y = swiglu_ffn(X, W13, W2)[0]
+    s2 = 2.0 * 0.5 * (1.0 + math.tanh(1.0))  # silu(2) in the tanh form
+    assert abs(y[0] - 3.0 * s2) < 1e-12 and abs(y[1] - 3.0 * s2) < 1e-12
+    assert abs(y[0] - 2.0 * 3.0 * 0.5 * (1.0 + math.tanh(1.5))) > 0.1

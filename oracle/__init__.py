@@ -28,7 +28,8 @@ the plain reading listed in each function's docstring.
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, exhaustive enumeration, library routines or brute force.
 """
-from .formats import decode_mxfp4, decode_q4_0, decode_blocks, e2m1_value, e8m0_scale  # noqa: F401
+from .formats import (decode_blocks, decode_mxfp4, decode_mxfp8, decode_nvfp4,  # noqa: F401
+                      decode_q4_0, e2m1_value, e4m3_value, e8m0_scale)
 from .route import route  # noqa: F401
 from .permute import permute  # noqa: F401
 from .ffn import combine, expert_ffn, silu, swiglu_ffn  # noqa: F401

@@ -67,6 +67,53 @@ def decode_mxfp4(blocks: np.ndarray) -> np.ndarray:
     return w.reshape(*blocks.shape[:-2], blocks.shape[-2] * BLOCK)
 
 
+# ----------------------------------------------------------------------------- next formats
+# The architecture walkthrough §五/§六 lists more bank formats than the two the layer
+# runs on.  These decoders are the oracle side of two of them; the CUDA kernels do
+# not read them yet.
+#
+# * NVFP4 (reading): 16 E2M1 elements share one E4M3 scale byte, and a whole weight
+#   matrix shares one fp32 tensor scale; weight = E2M1(c) * E4M3(s) * tensor_scale.
+#   A block stores its scale byte, then 8 code bytes: element i < 8 is the low nibble
+#   of code byte i and i >= 8 the high nibble of byte i - 8 (the Q4_0 order at half
+#   the block length).
+# * MXFP8 (OCP MX v1.0, E4M3 elements): 32 E4M3 elements share one E8M0 scale;
+#   a block stores the scale byte, then the 32 element bytes in order.
+NVFP4_BLOCK = 16
+
+
+def e4m3_value(byte) -> np.ndarray:
+    """E4M3 byte (OCP FP8 E4M3: bit 7 sign, bits 6..3 exponent with bias 7, bits 2..0
+    mantissa; no infinities, exponent and mantissa all ones is NaN) -> fp64.
+    Exponent field 0 is subnormal: m / 8 * 2^-6."""
+    b = np.asarray(byte, dtype=np.int64)
+    s = (b >> 7) & 1
+    e = (b >> 3) & 15
+    m = b & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, np.exp2(e - 7.0) * (1.0 + m / 8.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
+def decode_nvfp4(blocks: np.ndarray, tensor_scale: float) -> np.ndarray:
+    """NVFP4 blocks uint8 [..., nb, 9] and the matrix's fp32 tensor scale ->
+    weights fp64 [..., nb * 16]."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    assert blocks.shape[-1] == 9
+    qs = blocks[..., 1:9]
+    codes = np.concatenate([qs & 0x0F, qs >> 4], axis=-1).astype(np.int64)
+    w = e2m1_value(codes) * e4m3_value(blocks[..., 0])[..., None] * float(np.float32(tensor_scale))
+    return w.reshape(*blocks.shape[:-2], blocks.shape[-2] * NVFP4_BLOCK)
+
+
+def decode_mxfp8(blocks: np.ndarray) -> np.ndarray:
+    """MXFP8 (E4M3) blocks uint8 [..., nb, 33] -> weights fp64 [..., nb * 32]."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    assert blocks.shape[-1] == 33
+    w = e4m3_value(blocks[..., 1:33]) * e8m0_scale(blocks[..., 0])[..., None]
+    return w.reshape(*blocks.shape[:-2], blocks.shape[-2] * BLOCK)
+
+
 def decode_blocks(blocks: np.ndarray, qtype: str) -> np.ndarray:
     if qtype == "q4_0":
         return decode_q4_0(blocks)

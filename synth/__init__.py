@@ -17,6 +17,8 @@ from .gen import (  # noqa: F401
     gen_expert_weights,
     make_layer,
     quantize_mxfp4,
+    quantize_mxfp8,
+    quantize_nvfp4,
     quantize_q4_0,
     stream_trace,
     zipf_bias,

@@ -157,6 +157,90 @@ def quantize_mxfp4(w: np.ndarray) -> np.ndarray:
     return out.reshape(*lead, K // BLOCK, 17)
 
 
+def _e4m3_grid() -> np.ndarray:
+    """The 127 finite non-negative E4M3 values in code order (codes 0x00..0x7E)."""
+    c = np.arange(127)
+    e, m = c >> 3, c & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, np.exp2(e - 7.0) * (1.0 + m / 8.0))
+
+
+_E4M3 = _e4m3_grid()
+
+
+def _round_e4m3(x: np.ndarray) -> np.ndarray:
+    """Codes (uint8, sign in bit 7) of the E4M3 values nearest to x, ties to the even
+    code, saturating at 448."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.minimum(np.abs(x), 448.0).reshape(-1)
+    out = np.empty(mag.shape, dtype=np.uint8)
+    for i in range(0, mag.size, 1 << 16):
+        v = mag[i:i + (1 << 16)]
+        hi = np.clip(np.searchsorted(_E4M3, v, side="left"), 0, 126)
+        lo = np.clip(hi - 1, 0, 126)
+        dlo, dhi = np.abs(v - _E4M3[lo]), np.abs(_E4M3[hi] - v)
+        c = np.where(dhi < dlo, hi, lo)
+        c = np.where((dhi == dlo) & (hi != lo), np.where(lo % 2 == 0, lo, hi), c)
+        out[i:i + (1 << 16)] = c
+    sign = ((x.reshape(-1) < 0) & (out != 0)).astype(np.uint8)
+    return (out | (sign << 7)).reshape(x.shape)
+
+
+def quantize_nvfp4(w: np.ndarray):
+    """Encode float32 [..., K] (K % 16 == 0) into NVFP4: blocks uint8 [..., K/16, 9] and
+    one fp32 tensor scale for the whole array.
+
+    tensor_scale = amax / (6 * 448) (1 for an all-zero array); per 16-element block the
+    scale byte is the E4M3 value nearest to block_amax / 6 / tensor_scale; each element
+    x / (scale * tensor_scale) goes to the nearest E2M1 magnitude (ties to the even
+    code), saturating at 6.  Element i < 8 is the low nibble of code byte i."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    assert K % 16 == 0
+    lead = w.shape[:-1]
+    b = w.reshape(-1, 16).astype(np.float64)
+    n = b.shape[0]
+    amax = float(np.max(np.abs(b))) if b.size else 0.0
+    ts = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+    sbyte = _round_e4m3(np.max(np.abs(b), axis=1) / 6.0 / float(ts))
+    sval = np.where(sbyte == 0, 0.0, _E4M3[sbyte & 0x7F])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(sval[:, None] > 0, b / (sval[:, None] * float(ts)), 0.0)
+    mag = np.minimum(np.abs(v), 6.0)
+    dist = np.abs(mag[..., None] - _E2M1_GRID)
+    c = np.argmin(dist, axis=-1)
+    c1 = np.minimum(c + 1, 7)
+    tie = (np.take_along_axis(dist, c1[..., None], -1)[..., 0] == np.take_along_axis(dist, c[..., None], -1)[..., 0]) & (c1 != c)
+    c = np.where(tie & (c % 2 == 1), c1, c)
+    sign = ((v < 0) & (c != 0)).astype(np.uint8)
+    code = (c.astype(np.uint8) | (sign << 3)).astype(np.uint8)
+    out = np.empty((n, 9), dtype=np.uint8)
+    out[:, 0] = sbyte
+    out[:, 1:9] = code[:, :8] | (code[:, 8:] << 4)
+    return out.reshape(*lead, K // 16, 9), float(ts)
+
+
+def quantize_mxfp8(w: np.ndarray) -> np.ndarray:
+    """Encode float32 [..., K] into MXFP8 (E4M3) blocks uint8 [..., K/32, 33].
+
+    Per block: shared exponent u = floor(log2(amax)) - 8 clamped to [-127, 127] (scale
+    byte u + 127; amax == 0 gives byte 127 and zero elements); each element x / 2^u is
+    rounded to the nearest E4M3 value (ties to the even code), saturating at 448."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    assert K % BLOCK == 0
+    lead = w.shape[:-1]
+    b = w.reshape(-1, BLOCK).astype(np.float64)
+    n = b.shape[0]
+    amax = np.max(np.abs(b), axis=1)
+    with np.errstate(divide="ignore"):
+        u = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, 0.0)
+    u = np.clip(u, -127, 127)
+    out = np.empty((n, 33), dtype=np.uint8)
+    out[:, 0] = (u + 127).astype(np.uint8)
+    out[:, 1:] = _round_e4m3(b / np.exp2(u)[:, None])
+    return out.reshape(*lead, K // BLOCK, 33)
+
+
 _ENCODERS = {"q4_0": quantize_q4_0, "mxfp4": quantize_mxfp4}
 
 

@@ -50,3 +50,18 @@ def test_mxfp4_blocks():
     for blk, want in _blocks("mxfp4_blocks.txt"):
         got = oracle.decode_mxfp4(blk.reshape(1, 17))
         assert np.array_equal(got, want)
+
+
+def test_nvfp4_blocks():
+    rows = _rows("nvfp4_blocks.txt")
+    ts = float(rows[0][1])
+    for blk, want in [(np.frombuffer(bytes.fromhex(rows[1][1]), dtype=np.uint8),
+                       np.array(rows[2][1:], dtype=np.float64))]:
+        got = oracle.decode_nvfp4(blk.reshape(1, 9), ts)
+        assert np.array_equal(got, want)
+
+
+def test_mxfp8_blocks():
+    for blk, want in _blocks("mxfp8_blocks.txt"):
+        got = oracle.decode_mxfp8(blk.reshape(1, 33))
+        assert np.array_equal(got, want) and np.array_equal(np.signbit(got), np.signbit(want))

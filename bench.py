@@ -291,7 +291,8 @@ def main():
 
     # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
     stream_res = pstream = None
-    if args.config == "decode" and (args.stream_steps > 0 or args.prefill_stream_chunks > 0):
+    # (one replica only: the 16 GB pinned bank is host memory, shared by all ranks of a node)
+    if args.config == "decode" and world == 1 and (args.stream_steps > 0 or args.prefill_stream_chunks > 0):
         ctx = stream_bank(L, dev)
         if args.stream_steps > 0:
             stream_res = measure_stream(L, dev, args.stream_steps, 16, rank, ctx)

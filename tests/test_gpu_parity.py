@@ -251,7 +251,7 @@ def test_decode_batch_invariance(env, path):
 @pytest.mark.parametrize("qtype", ["q4_0", "mxfp4"])
 def test_gemm_decode_path_ragged_shared_and_multi_tile(env, qtype):
     """Decode GEMM on ragged H / I (partial 128-row tiles, half-filled last block), a shared
-    expert, and experts with more rows than one 32-token tile."""
+    expert, and experts with more rows than one token tile."""
     L = make_layer(H=224, I=96, E=5, k=3, T=60, qtype=qtype, seed=13, shared=True, zipf=1.0)
     _, out, ids, _ = _layer_gpu(env, L, path=3)
     r = oracle.layer(L.x, L.logits, L.k, L.qtype, L.w13, L.w2, L.shared_w13, L.shared_w2)

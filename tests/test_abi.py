@@ -58,3 +58,32 @@ def test_invalid_arguments_rejected_on_host(F):
     with pytest.raises(F.FtmoeError):
         F.ftmoe_gate(0, 0, 4, 64, 8, 0, stream=0)  # null pointers
     F.ftmoe_gate(0, 0, 0, 64, 8, 0, stream=0)
+
+
+def test_cache_descriptor_checked_on_host(F):
+    """A malformed cache descriptor is refused before anything touches the GPU."""
+    good = dict(layers=2, E=8, blob_bytes=1024, bank=1, pool=1, slots_per_layer=2, policy=0,
+                copy_stream=1)
+    bad = [dict(layers=0), dict(E=0), dict(slots_per_layer=0), dict(bank=None), dict(pool=None),
+           dict(blob_bytes=0), dict(blob_bytes=1000), dict(copy_stream=None), dict(policy=2)]
+    for b in bad:
+        d = dict(good, **b)
+        desc = F.ftmoe_cache_desc(d["layers"], d["E"], d["blob_bytes"], d["bank"], d["pool"],
+                                  d["slots_per_layer"], d["policy"], d["copy_stream"])
+        h = ctypes.c_void_p()
+        assert F.lib.ftmoe_cache_create(ctypes.byref(desc), ctypes.byref(h)) == 1, b
+        assert not h.value
+    assert F.lib.ftmoe_cache_create(None, None) == 1
+    # the other cache calls refuse a null handle
+    n = ctypes.c_int(0)
+    assert F.lib.ftmoe_cache_prefetch_history(None, 0, None, ctypes.byref(n), None, None) == 1
+    assert F.lib.ftmoe_cache_release(None, 0, None) == 1
+    assert F.lib.ftmoe_cache_destroy(None) == 1
+
+
+def test_workspace_sizes_grow_with_the_problem(F):
+    a = F.ftmoe_layer_workspace_bytes(64, 8, 128, 2048, 768, 0)
+    b = F.ftmoe_layer_workspace_bytes(4096, 8, 128, 2048, 768, 0)
+    c = F.ftmoe_layer_workspace_bytes(64, 8, 128, 2048, 768, 1)  # with a shared expert
+    assert 0 < a < b and c > a
+    assert F.ftmoe_ffn_workspace_bytes(64, 8, 128, 2048, 768) <= a

@@ -309,41 +309,56 @@ def main():
         cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"one oracle layer pass over {sample_T} tokens of the workload ({dt:.1f} s)"}
 
-    launches_per_step = 1 + (1 if P <= 16384 else 3) + 2 + 1 + (2 if L.shared_w13 is not None else 0)
     if rank == 0:
-        line = {
-            "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(head["step_ms"])),
-            "eager_ms_per_step": head["eager_ms"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
-            "config": {"workload": cfg["workload"], "H": H, "I": I, "E": E, "k": k, "T": T,
-                       "qtype": L.qtype, "parallelism": f"replicas{world}", "ffn_path": args.ffn_path,
-                       "l2": "flushed between steps (512 MB write)",
-                       "step": "whole layer replayed from a CUDA graph"},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_serial, "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2,
-                    "how": "per step: pinned host x and logits copied in, the layer, the output "
-                           "copied back, one CUDA graph, L2 flushed between steps like the device-"
-                           "timed value",
-                    "pipelined_value": e2e_val,
-                    "pipelined_how": "the same copies every step through two device buffers, so "
-                                     "that step s's copies overlap its neighbours' layers; no L2 "
-                                     "flush between these steps, so part of the weights stays in "
-                                     "L2 and this can exceed the device-timed value"},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
-            "decode_sweep": sweep or None,
-            "prefill": prefill,
-            "stream": stream_res,
-            "prefill_stream": pstream,
-            "gate": gate,
-        }
+        line = result_line(
+            args, world, cfg, L, value=value, step_ms=head["step_ms"], eager_ms=head["eager_ms"],
+            roofline=roofline, cpu=cpu, e2e_serial=e2e_serial, e2e_pipelined=e2e_val,
+            clocks=clk.summary(),
+            extras={"decode_sweep": sweep or None, "prefill": prefill, "stream": stream_res,
+                    "prefill_stream": pstream, "gate": gate})
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def launches_per_step(P: int, shared: bool) -> int:
+    """Kernels of one layer step: route, permute (one kernel up to 16384 pairs, else
+    count / scan / scatter), the expert FFN's two projections, combine, and the shared
+    expert's two projections."""
+    return 1 + (1 if P <= 16384 else 3) + 2 + 1 + (2 if shared else 0)
+
+
+def result_line(args, world, cfg, L, value, step_ms, eager_ms, roofline, cpu, e2e_serial,
+                e2e_pipelined, clocks, extras):
+    """The bench's one JSON line (rank 0)."""
+    T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
+    line = {
+        "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(step_ms)),
+        "eager_ms_per_step": eager_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations / logits, N(0,0.02) weights quantized)",
+        "config": {"workload": cfg["workload"], "H": H, "I": I, "E": E, "k": k, "T": T,
+                   "qtype": L.qtype, "parallelism": f"replicas{world}", "ffn_path": args.ffn_path,
+                   "l2": "flushed between steps (512 MB write)",
+                   "step": "whole layer replayed from a CUDA graph"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_serial, "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2,
+                "how": "per step: pinned host x and logits copied in, the layer, the output "
+                       "copied back, one CUDA graph, L2 flushed between steps like the device-"
+                       "timed value",
+                "pipelined_value": e2e_pipelined,
+                "pipelined_how": "the same copies every step through two device buffers, so "
+                                 "that step s's copies overlap its neighbours' layers; no L2 "
+                                 "flush between these steps, so part of the weights stays in "
+                                 "L2 and this can exceed the device-timed value"},
+        "gpu_launches": launches_per_step(T * k, L.shared_w13 is not None) * args.steps,
+        "clocks": clocks,
+    }
+    line.update(extras)
+    return line
 
 
 def measure_gate(dev, T, H, E, flush, stream, pk, pk_kind, reps):

@@ -6,6 +6,12 @@ experts, top-8, Q4_0) at a batch of 64 tokens.  One step = one full layer pass
 HBM.  Between timed steps a 512 MB buffer is written to flush the 126 MB L2, and
 only the layer itself sits inside the per-step CUDA events.
 
+The same JSON line also carries: the end-to-end figure with pinned host copies, the
+decode sweep (T = 1, 4, 16), the 4096-token prefill layer (Q4_0 and MXFP4), the router
+gate, batch-1 decode through 48 layers streamed from a pinned expert bank (ids known
+one layer ahead, on demand, predicted from history), chunked prefill with the whole
+bank streamed, and the oracle's CPU throughput.
+
 --impl reference times the fp64 CPU oracle on the same workload instead.
 Multi-GPU (torchrun): independent replicas, one per rank, no collective on the
 data path; value = tokens of all ranks / max over ranks of the timed region.

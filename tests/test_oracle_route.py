@@ -66,3 +66,18 @@ def test_rejects_bad_k_and_nonfinite():
         route(np.zeros((1, 4), np.float32), 5)
     with pytest.raises(ValueError):
         route(np.array([[0.0, np.inf]], np.float32), 1)
+
+
+def test_large_e_matches_library_sort_and_softmax():
+    """E = 1024, k = 32 with many exact ties: the selection equals the library's
+    lexicographic sort on (descending logit, ascending id), and the weights equal the
+    library softmax of the selected logits (a softmax renormalised over a subset is
+    the softmax of that subset)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(8)
+    lg = np.round(rng.standard_normal((16, 1024)) * 4).astype(np.float32) / 4  # quarter steps: ties
+    ids, w = route(lg, 32)
+    for t in range(16):
+        order = np.lexsort((np.arange(1024), -lg[t].astype(np.float64)))[:32]
+        assert np.array_equal(ids[t], order)
+        assert np.allclose(w[t], softmax(lg[t, order].astype(np.float64)), rtol=1e-12, atol=0)

@@ -40,3 +40,43 @@ def test_global_pool_is_shared_across_layers():
     assert c.request(1, [1]) == [(1, True)]
     assert c.request(1, [2]) == [(0, True)]  # evicts layer 0's expert 1 (oldest)
     assert c.request(0, [1]) == [(1, True)]
+
+
+def _textbook_lru_misses(trace, capacity, shared):
+    """Hit/miss sequence of a textbook LRU (an ordered dict: a hit moves to the most recent
+    end, a miss evicts the least recent entry when full) over the same touches."""
+    from collections import OrderedDict
+    caches = {}
+    out = []
+    for layer, ids in trace:
+        c = caches.setdefault(None if shared else layer, OrderedDict())
+        for e in ids:
+            key = (layer, int(e))
+            if key in c:
+                c.move_to_end(key)
+                out.append(False)
+            else:
+                if len(c) >= capacity:
+                    c.popitem(last=False)
+                c[key] = True
+                out.append(True)
+    return out
+
+
+@pytest.mark.parametrize("policy", ["layer", "global"])
+def test_misses_equal_a_textbook_lru(policy):
+    """Slot numbering aside, the simulator is an LRU: its hit / miss sequence equals an
+    independent ordered-dict LRU's on random traces with repeats (requests never larger
+    than a pool, so the same-request rule never binds differently)."""
+    import numpy as np
+    rng = np.random.default_rng(4)
+    layers, E, slots, k = 3, 12, 4, 3
+    sim = LRUSim(layers, E, slots, policy)
+    trace = []
+    for _ in range(400):
+        layer = int(rng.integers(layers))
+        ids = rng.choice(E, size=k, replace=False, p=np.arange(E, 0, -1) / np.arange(E, 0, -1).sum())
+        trace.append((layer, ids))
+    got = [copied for layer, ids in trace for _, copied in sim.request(layer, ids)]
+    cap = slots if policy == "layer" else slots * layers
+    assert got == _textbook_lru_misses(trace, cap, policy == "global")

@@ -116,6 +116,24 @@ ftmoe_status ftmoe_repack(int qtype, const void* canon, void* tiles, int E, int 
 ftmoe_status ftmoe_dequant(int qtype, const void* tiles, int E, int N, int K, float* out,
                            ftmoe_stream_t stream);
 
+/* Tensor-core operands built from the tiles (verification aid, [P5] §六 GGUF dequant):
+ * which of the FFN kernels' decode steps to reproduce.  Each runs the same device
+ * functions as that kernel and reads the result back through that kernel's layout. */
+typedef enum {
+  FTMOE_OPERAND_PREFILL = 0, /* prefill grouped GEMM A tile: each weight rounded once to
+                                bf16, round-to-nearest-even of the exact decoded value
+                                ((q - 8) * d for Q4_0, E2M1 * 2^(e - 127) for MXFP4);
+                                beyond the bf16 range -> +-inf; NaN scales -> NaN */
+  FTMOE_OPERAND_CODES = 1    /* decode GEMM A operand: the unscaled code value, q - 8
+                                (Q4_0) or the E2M1 value (MXFP4), exact */
+} ftmoe_operand;
+
+/* Writes operand `which` of tiles (device) as bf16 bit patterns out[E][N][K] (device,
+ * 16-byte aligned).  Same argument rules as ftmoe_dequant; an unknown `which` or a
+ * misaligned `out` returns FTMOE_ERR_INVALID_ARG. */
+ftmoe_status ftmoe_dequant_operand(int qtype, int which, const void* tiles, int E, int N, int K,
+                                   uint16_t* out, ftmoe_stream_t stream);
+
 /* ------------------------------------------------------------------ gate
  * The scores the router selects from ([P3] sparse expert activation), from the
  * hidden state: logits[t][e] = sum over h of x[t][h] * wg[e][h].
@@ -258,9 +276,14 @@ ftmoe_status ftmoe_check_wait_timeout(long long limit_ns, int* waited_ok, ftmoe_
  * slots_per_layer slots per layer; FTMOE_LRU_GLOBAL shares all slots among
  * all layers.  Every request touches its ids in order with a new recency stamp;
  * a resident expert is a hit, a missing one is copied into the lowest empty
- * slot of its pool, else the least recently used slot not touched by the same
- * request (none left -> FTMOE_ERR_NO_SLOT).  Copies go on `copy_stream` and a
- * slot is not overwritten before the compute work released on it finished.
+ * slot of its pool, else the least recently used slot that is neither touched by
+ * the same request nor pinned.  An acquire pins the slots it touched until the
+ * layer's ftmoe_cache_release ([P4] 核心洞察: a layer, possibly replayed as a CUDA
+ * graph, reads its experts in place), so no later prefetch or acquire overwrites
+ * them; a prefetch pins nothing.  A request that finds no slot for a missing id
+ * returns FTMOE_ERR_NO_SLOT and changes nothing (no slot, stamp or copy).  Copies
+ * go on `copy_stream` and a slot is not overwritten before the compute work
+ * released on it finished.
  */
 typedef enum { FTMOE_LRU_PER_LAYER = 0, FTMOE_LRU_GLOBAL = 1 } ftmoe_cache_policy;
 
@@ -303,16 +326,19 @@ ftmoe_status ftmoe_cache_prefetch(ftmoe_cache* c, int layer, const int32_t* ids,
 ftmoe_status ftmoe_cache_prefetch_history(ftmoe_cache* c, int layer, int32_t* ids_out, int* n_out,
                                           int32_t* slots_out, uint8_t* copied_out);
 
-/* Make `layer`'s experts ids[0..n) resident (copying misses) and make `compute`
- * wait for their copies.  blob_out: host array of E pointers, filled for the
- * requested ids (other entries untouched), ready for ftmoe_weights.expert_blob.
- * slots_out / copied_out as for prefetch. */
+/* Make `layer`'s experts ids[0..n) resident (copying misses), make `compute`
+ * wait for their copies and pin their slots until ftmoe_cache_release(layer).
+ * blob_out: host array of E pointers, filled for the requested ids (other entries
+ * untouched), ready for ftmoe_weights.expert_blob.  slots_out / copied_out as for
+ * prefetch.  FTMOE_ERR_NO_SLOT (nothing changed) when the pool has fewer unpinned
+ * slots than the request needs. */
 ftmoe_status ftmoe_cache_acquire(ftmoe_cache* c, int layer, const int32_t* ids, int n,
                                  ftmoe_stream_t compute, const void** blob_out,
                                  int32_t* slots_out, uint8_t* copied_out);
 
-/* Mark the slots acquired for `layer` as in use by the work enqueued on
- * `compute` so far; a later copy into one of them waits for that work. */
+/* Unpin the slots of every acquire of `layer` since its previous release and mark
+ * them as in use by the work enqueued on `compute` so far: a later copy into one of
+ * them waits for that work. */
 ftmoe_status ftmoe_cache_release(ftmoe_cache* c, int layer, ftmoe_stream_t compute);
 
 /* Counters; synchronizes the copy stream so that h2d_ms is complete. */

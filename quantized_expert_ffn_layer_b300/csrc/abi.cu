@@ -177,6 +177,14 @@ ftmoe_status ftmoe_dequant(int qtype, const void* tiles, int E, int N, int K, fl
   return from_cuda(launch_dequant(qtype, tiles, E, N, K, out, (cudaStream_t)stream));
 }
 
+ftmoe_status ftmoe_dequant_operand(int qtype, int which, const void* tiles, int E, int N, int K,
+                                   uint16_t* out, ftmoe_stream_t stream) {
+  if (!ftmoe_tiled_bytes(qtype, E, N, K) || !tiles || !out || ((uintptr_t)out & 15) ||
+      (which != FTMOE_OPERAND_PREFILL && which != FTMOE_OPERAND_CODES))
+    return FTMOE_ERR_INVALID_ARG;
+  return from_cuda(launch_operand(qtype, which, tiles, E, N, K, out, (cudaStream_t)stream));
+}
+
 ftmoe_status ftmoe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          ftmoe_stream_t stream) {
   if (!tke_ok(T, k, E)) return FTMOE_ERR_INVALID_ARG;

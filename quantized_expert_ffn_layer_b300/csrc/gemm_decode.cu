@@ -41,6 +41,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
+#include "operand.cuh"
 #include "tcgen05.cuh"
 
 namespace ftmoe {
@@ -182,65 +183,6 @@ __device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const Gem
 }
 
 // ---------------------------------------------------------------- weight decode
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t saddr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
-  return v;
-}
-
-
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(saddr)
-               : "memory");
-  return v;
-}
-
-// bf16x2 codes of elements (0, 1) and (2, 3) of a 4-element group from a word whose
-// bytes hold the group's 4-bit codes in the order (e0, e2, e1, e3), one per low nibble:
-// q - 8 for Q4_0 (the byte 0x43 above a code byte is bf16 128 + q; one bf16x2 subtract
-// of 136), the E2M1 value for MXFP4.  Both are exact in bf16.
-template <int QT>
-__device__ __forceinline__ void decode_plain(uint32_t E, uint32_t& o0, uint32_t& o1) {
-  if (QT == FTMOE_Q4_0) {
-    const uint32_t K = 0x43434343u;
-    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-    uint32_t t0 = prmt(E, K, 0x4240u), t1 = prmt(E, K, 0x4341u);
-    const __nv_bfloat162 u0 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t0), off);
-    const __nv_bfloat162 u1 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t1), off);
-    o0 = *reinterpret_cast<const uint32_t*>(&u0);
-    o1 = *reinterpret_cast<const uint32_t*>(&u1);
-  } else {
-    const uint32_t TWO126 = 0x7E807E80u;
-    const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
-    uint32_t r[2];
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      // ((c & 7) << 6) | ((c & 8) << 12) read as bf16 is E2M1(c) * 2^-126 (the E2M1
-      // subnormal lands on a bf16 subnormal); one bf16 multiply by 2^126 makes it exact
-      uint32_t t = ((v[p] & 0x00070007u) << 6) | ((v[p] & 0x00080008u) << 12);
-      const __nv_bfloat162 w = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
-      r[p] = *reinterpret_cast<const uint32_t*>(&w);
-    }
-    o0 = r[0];
-    o1 = r[1];
-  }
-}
-
 // One converter warp decodes a 16-row x 64-element record into its 16 tensor-memory
 // lanes (the A tile rows of the record) at `taddr`.  Lane L = 4g + c reads its own 16
 // bytes: word j holds elements 16j + 4c + (0..3) of row g in the low nibbles (bytes in

@@ -27,9 +27,8 @@
 // ordered expert by expert with the token tile innermost, so CTAs that run at the
 // same time share weight tiles through L2.
 //
-// A-tile row order: weight row r of a 16-row record is stored at tile row
-// sigma(r) (rows 0..3 -> 0,2,4,6, rows 4..7 -> 1,3,5,7, and the same +8 for rows
-// 8..15).  With it the converter stores of a quarter-warp fall on 8 different
+// A-tile row order: weight row r of a 16-row record is stored at tile row sigma(r)
+// (operand.cuh), so that the converter stores of a quarter-warp fall on 8 different
 // 16-byte bank groups of the swizzled rows; the epilogue maps TMEM lanes back.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,6 +38,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
+#include "operand.cuh"
 #include "tcgen05.cuh"
 
 namespace ftmoe {
@@ -151,170 +151,6 @@ __device__ __forceinline__ int gm_record_row(const GmItem& it, int ri, const Gem
   const int row = it.f0 + (ri & 7) * 16;
   ok = row < a.nrows;
   return (MODE == 0 && (ri >> 3)) ? row + a.up_row0 : row;
-}
-
-__host__ __device__ constexpr int gm_sigma(int r) {
-  return (r & 8) | ((r & 7) < 4 ? 2 * (r & 3) : 2 * (r & 3) + 1);
-}
-__device__ __forceinline__ int gm_sigma_inv(int t) {
-  const int u = t & 7;
-  return (t & 8) | ((u & 1) ? 4 + (u >> 1) : (u >> 1));
-}
-
-// ---------------------------------------------------------------- weight decode
-// W holds 8 four-bit codes of one row as nibble slots (0,4,2,6,1,5,3,7) = elements
-// 0..7; slots p and p + 4 form the bf16x2 pair p.  Returns the 8 bf16 in element
-// order.  Q4_0: (q - 8) * d rounded once to bf16, with d = dhi + dlo split so that
-// (q - 8) * dlo is exact and the fused multiply-add rounds the exact product.
-// MXFP4: E2M1 value times 2^(e - 127), exact unless it leaves the bf16 range.
-template <int QT>
-__device__ __forceinline__ uint4 decode8(uint32_t W, uint32_t s_hi, uint32_t s_lo) {
-  uint32_t r[4];
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t v = (W >> (4 * p)) & 0x000F000Fu;
-    if (QT == FTMOE_Q4_0) {
-      uint32_t t = v | 0x43004300u;  // bf16 128 + q
-      const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-      const __nv_bfloat162 u = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), off);  // q - 8
-      const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
-      const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
-      r[p] = *reinterpret_cast<const uint32_t*>(&w);
-    } else {
-      uint32_t t = ((v & 0x00070007u) << 6) | ((v & 0x00080008u) << 12);  // E2M1 * 2^-126
-      const uint32_t TWO126 = 0x7E807E80u;
-      __nv_bfloat162 w = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&t),
-                                 *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
-      w = __hmul2(w, *reinterpret_cast<const __nv_bfloat162*>(&s_hi));
-      r[p] = *reinterpret_cast<const uint32_t*>(&w);
-    }
-  }
-  return make_uint4(r[0], r[2], r[1], r[3]);
-}
-
-// Block scale of one row as (hi, lo) bf16x2 pairs with hi + lo == the scale exactly
-// (Q4_0 fp16 d), or (2^(e-127), 0) for an MXFP4 E8M0 byte.
-template <int QT>
-__device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
-  if (QT == FTMOE_Q4_0) {
-    const float d = half_bits_to_f32(bits);
-    const uint32_t hi = f32_to_bf16_bits(d);
-    const uint32_t lo = f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
-    hi2 = hi | (hi << 16);
-    lo2 = lo | (lo << 16);
-  } else {
-    const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
-    hi2 = b | (b << 16);
-    lo2 = 0;
-  }
-}
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(saddr)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// Four bf16x2 (128 + q) pairs from nibble bytes: E1 holds elements 0..3 and E2 elements
-// 4..7 of one row as byte-aligned nibbles in the order (e0, e2, e1, e3).
-__device__ __forceinline__ void q4_pairs(uint32_t E1, uint32_t E2, uint32_t (&t)[4]) {
-  const uint32_t K = 0x43434343u;  // high byte of bf16 128
-  t[0] = prmt(E1, K, 0x4240u);
-  t[1] = prmt(E1, K, 0x4341u);
-  t[2] = prmt(E2, K, 0x4240u);
-  t[3] = prmt(E2, K, 0x4341u);
-}
-
-// (128 + q) pairs -> RNE((q - 8) * d) with d = hi + lo split exactly (see row_scale).
-__device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi, uint32_t s_lo) {
-  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-  uint32_t r[4];
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const __nv_bfloat162 u = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t[p]), off);
-    const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
-    const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
-    r[p] = *reinterpret_cast<const uint32_t*>(&w);
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
-}
-
-// One converter thread's share of a record in shared memory.  Record lanes 4g + 2m (A)
-// and 4g + 2m + 1 (B) hold elements 8m..8m+7 of each 16-element step j of rows g and
-// g + 8 (A: elements 8m..8m+3, B: 8m+4..8m+7).  The thread decodes NSTEP steps starting
-// at J0 (NSTEP = 2: quantization block J0 / 2; NSTEP = 1: one step) of both rows into the
-// A tile.  Lane pairs (m = 0, 1) share the scale conversions through one shuffle.  The
-// two 16-byte code loads are issued in an order that depends on (g >> 1) & 1 so that
-// each quarter-warp reads 8 different bank groups.
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ void convert_record(uint32_t rec, uint32_t tile, int rg, int g, int m) {
-  constexpr int BLK = J0 >> 1;  // quantization block of the thread's steps
-  const int sw = (g >> 1) & 1;
-  const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
-  const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
-  const uint4 ca = sw ? l2 : l1, cb = sw ? l1 : l2;
-  const int T0 = rg * 16 + gm_sigma(g);  // tile row of record row g (row g + 8: T0 + 8)
-  const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
-  const uint32_t row1 = row0 + 1024;
-  const uint32_t ph = (uint32_t)(T0 & 7);
-  // scale of row g + 8 m (this lane) and of the other row (partner lane)
-  uint32_t sbits;
-  {
-    const int idx = (g * 2 + BLK) * 2 + m;
-    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
-    uint32_t w;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(rec + REC_CODE_BYTES + (byte & ~3)) : "memory");
-    sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
-  }
-  uint32_t mh, ml;
-  row_scale<QT>(sbits, mh, ml);
-  const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
-  const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
-  const uint32_t sh0 = m ? oh : mh, sl0 = m ? ol : ml;
-  const uint32_t sh1 = m ? mh : oh, sl1 = m ? ml : ol;
-  const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-  const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-#pragma unroll
-  for (int s = 0; s < NSTEP; ++s) {
-    const int j = J0 + s;
-    const uint32_t A = wa[j], Bw = wb[j];
-    const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
-    if (QT == FTMOE_Q4_0) {
-      uint32_t t0[4], t1[4];
-      q4_pairs(A & 0x0F0F0F0Fu, Bw & 0x0F0F0F0Fu, t0);                // row g
-      q4_pairs((A >> 4) & 0x0F0F0F0Fu, (Bw >> 4) & 0x0F0F0F0Fu, t1);  // row g + 8
-      sts128(row0 + off, q4_scale(t0, sh0, sl0));
-      sts128(row1 + off, q4_scale(t1, sh1, sl1));
-    } else {
-      const uint32_t wg = (A & 0x0F0F0F0Fu) | ((Bw & 0x0F0F0F0Fu) << 4);
-      const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (Bw & 0xF0F0F0F0u);
-      sts128(row0 + off, decode8<QT>(wg, sh0, sl0));
-      sts128(row1 + off, decode8<QT>(wg8, sh1, sl1));
-    }
-  }
 }
 
 // 16-byte global -> shared copy (LDGSTS); src_bytes = 0 writes zeros.
@@ -527,14 +363,14 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
           const uint32_t tile = base_addr + slot * C::STAGE + (ri >> 3) * GM_A_TILE;
           if (MODE == 0) {
-            if (jsel) convert_record<QT, 2, 2>(rec, tile, ri & 7, g, m);
-            else convert_record<QT, 2, 0>(rec, tile, ri & 7, g, m);
+            if (jsel) convert_record_swizzled<QT, 2, 2>(rec, tile, ri & 7, g, m);
+            else convert_record_swizzled<QT, 2, 0>(rec, tile, ri & 7, g, m);
           } else {
             switch (jsel) {
-              case 0: convert_record<QT, 1, 0>(rec, tile, ri & 7, g, m); break;
-              case 1: convert_record<QT, 1, 1>(rec, tile, ri & 7, g, m); break;
-              case 2: convert_record<QT, 1, 2>(rec, tile, ri & 7, g, m); break;
-              default: convert_record<QT, 1, 3>(rec, tile, ri & 7, g, m); break;
+              case 0: convert_record_swizzled<QT, 1, 0>(rec, tile, ri & 7, g, m); break;
+              case 1: convert_record_swizzled<QT, 1, 1>(rec, tile, ri & 7, g, m); break;
+              case 2: convert_record_swizzled<QT, 1, 2>(rec, tile, ri & 7, g, m); break;
+              default: convert_record_swizzled<QT, 1, 3>(rec, tile, ri & 7, g, m); break;
             }
           }
         }

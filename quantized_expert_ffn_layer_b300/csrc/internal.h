@@ -34,6 +34,8 @@ cudaError_t launch_repack(int qtype, const void* canon, void* tiles, int E, int 
                           cudaStream_t st);
 cudaError_t launch_dequant(int qtype, const void* tiles, int E, int N, int K, float* out,
                            cudaStream_t st);
+cudaError_t launch_operand(int qtype, int which, const void* tiles, int E, int N, int K,
+                           uint16_t* out, cudaStream_t st);
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          cudaStream_t st);

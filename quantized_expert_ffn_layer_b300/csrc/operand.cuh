@@ -1,0 +1,217 @@
+// Tensor-core operand decode of the tiled 4-bit weight records (the GGUF dequant of the
+// FreeToken architecture walkthrough §六, for the Q4_0 / MXFP4 banks of §五).
+//
+// Two operand forms, each used by one tcgen05 kernel and reproduced element by element
+// by the verification kernels in operand_check.cu (ftmoe_dequant_operand):
+//   * the prefill grouped GEMM's A tile: every weight rounded once to bf16
+//     (round-to-nearest-even of the exact decoded value) in the 128-byte-swizzled
+//     K-major layout (convert_record_swizzled);
+//   * the decode GEMM's A operand: the unscaled code value (q - 8 for Q4_0, the E2M1
+//     value for MXFP4), exact in bf16 (decode_plain).
+// Record layout: see common.cuh.
+#pragma once
+
+#include "common.cuh"
+#include "pipeline.cuh"
+
+namespace ftmoe {
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t saddr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- prefill A tile
+// A-tile row order: weight row r of a 16-row record is stored at tile row sigma(r)
+// (rows 0..3 -> 0,2,4,6, rows 4..7 -> 1,3,5,7, and the same +8 for rows 8..15), so
+// that the converter stores of a quarter-warp fall on 8 different 16-byte bank groups.
+__host__ __device__ constexpr int gm_sigma(int r) {
+  return (r & 8) | ((r & 7) < 4 ? 2 * (r & 3) : 2 * (r & 3) + 1);
+}
+__host__ __device__ inline int gm_sigma_inv(int t) {
+  const int u = t & 7;
+  return (t & 8) | ((u & 1) ? 4 + (u >> 1) : (u >> 1));
+}
+
+// W holds 8 E2M1 codes of one row as nibble slots (0,4,2,6,1,5,3,7) = elements 0..7;
+// slots p and p + 4 form the bf16x2 pair p.  Returns the 8 values times the block
+// scale s_hi (2^(e - 127) as bf16x2) in element order: exact unless the product
+// leaves the bf16 range.
+__device__ __forceinline__ uint4 e2m1_scaled8(uint32_t W, uint32_t s_hi) {
+  uint32_t r[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t v = (W >> (4 * p)) & 0x000F000Fu;
+    uint32_t t = ((v & 0x00070007u) << 6) | ((v & 0x00080008u) << 12);  // E2M1 * 2^-126
+    const uint32_t TWO126 = 0x7E807E80u;
+    __nv_bfloat162 w = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&t),
+                               *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
+    w = __hmul2(w, *reinterpret_cast<const __nv_bfloat162*>(&s_hi));
+    r[p] = *reinterpret_cast<const uint32_t*>(&w);
+  }
+  return make_uint4(r[0], r[2], r[1], r[3]);
+}
+
+// Block scale of one row as (hi, lo) bf16x2 pairs with hi + lo == the scale exactly
+// (Q4_0 fp16 d; lo = 0 when d is not finite, so that +-inf scales give +-inf weights and
+// NaN only where the code is q = 8), or (2^(e-127), 0) for an MXFP4 E8M0 byte
+// (e = 0 is the subnormal 2^-127, e = 255 NaN).
+template <int QT>
+__device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
+  if (QT == FTMOE_Q4_0) {
+    const float d = half_bits_to_f32(bits);
+    const uint32_t hi = f32_to_bf16_bits(d);
+    const uint32_t lo = (bits & 0x7C00u) == 0x7C00u ? 0u : f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
+    hi2 = hi | (hi << 16);
+    lo2 = lo | (lo << 16);
+  } else {
+    const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
+    hi2 = b | (b << 16);
+    lo2 = 0;
+  }
+}
+
+// Four bf16x2 (128 + q) pairs from nibble bytes: E1 holds elements 0..3 and E2 elements
+// 4..7 of one row as byte-aligned nibbles in the order (e0, e2, e1, e3).
+__device__ __forceinline__ void q4_pairs(uint32_t E1, uint32_t E2, uint32_t (&t)[4]) {
+  const uint32_t K = 0x43434343u;  // high byte of bf16 128
+  t[0] = prmt(E1, K, 0x4240u);
+  t[1] = prmt(E1, K, 0x4341u);
+  t[2] = prmt(E2, K, 0x4240u);
+  t[3] = prmt(E2, K, 0x4341u);
+}
+
+// (128 + q) pairs -> RNE((q - 8) * d) with d = hi + lo split exactly (see row_scale):
+// (q - 8) * lo is exact in bf16 (at most 4 + 4 significant bits), so the one rounding
+// of the fused multiply-add is the rounding of the exact product.
+__device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi, uint32_t s_lo) {
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+  uint32_t r[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const __nv_bfloat162 u = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t[p]), off);
+    const __nv_bfloat162 lo = __hmul2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_lo));
+    const __nv_bfloat162 w = __hfma2(u, *reinterpret_cast<const __nv_bfloat162*>(&s_hi), lo);
+    r[p] = *reinterpret_cast<const uint32_t*>(&w);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// One converter thread's share of a record in shared memory.  Record lanes 4g + 2m (A)
+// and 4g + 2m + 1 (B) hold elements 8m..8m+7 of each 16-element step j of rows g and
+// g + 8 (A: elements 8m..8m+3, B: 8m+4..8m+7).  The thread decodes NSTEP steps starting
+// at J0 (NSTEP = 2: quantization block J0 / 2; NSTEP = 1: one step) of both rows into the
+// A tile at `tile` (128 rows of 64 bf16, 128-byte swizzle), record row group rg.  Lane
+// pairs (m = 0, 1) share the scale conversions through one shuffle, so all 32 lanes of
+// the warp must call it together.  The two 16-byte code loads are issued in an order
+// that depends on (g >> 1) & 1 so that each quarter-warp reads 8 different bank groups.
+template <int QT, int NSTEP, int J0>
+__device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t tile, int rg, int g,
+                                                        int m) {
+  constexpr int BLK = J0 >> 1;  // quantization block of the thread's steps
+  const int sw = (g >> 1) & 1;
+  const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
+  const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
+  const uint4 ca = sw ? l2 : l1, cb = sw ? l1 : l2;
+  const int T0 = rg * 16 + gm_sigma(g);  // tile row of record row g (row g + 8: T0 + 8)
+  const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
+  const uint32_t row1 = row0 + 1024;
+  const uint32_t ph = (uint32_t)(T0 & 7);
+  // scale of row g + 8 m (this lane) and of the other row (partner lane)
+  uint32_t sbits;
+  {
+    const int idx = (g * 2 + BLK) * 2 + m;
+    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
+    const uint32_t w = lds32(rec + REC_CODE_BYTES + (byte & ~3));
+    sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
+  }
+  uint32_t mh, ml;
+  row_scale<QT>(sbits, mh, ml);
+  const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
+  const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
+  const uint32_t sh0 = m ? oh : mh, sl0 = m ? ol : ml;
+  const uint32_t sh1 = m ? mh : oh, sl1 = m ? ml : ol;
+  const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+  const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+  for (int s = 0; s < NSTEP; ++s) {
+    const int j = J0 + s;
+    const uint32_t A = wa[j], Bw = wb[j];
+    const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
+    if (QT == FTMOE_Q4_0) {
+      uint32_t t0[4], t1[4];
+      q4_pairs(A & 0x0F0F0F0Fu, Bw & 0x0F0F0F0Fu, t0);                // row g
+      q4_pairs((A >> 4) & 0x0F0F0F0Fu, (Bw >> 4) & 0x0F0F0F0Fu, t1);  // row g + 8
+      sts128(row0 + off, q4_scale(t0, sh0, sl0));
+      sts128(row1 + off, q4_scale(t1, sh1, sl1));
+    } else {
+      const uint32_t wg = (A & 0x0F0F0F0Fu) | ((Bw & 0x0F0F0F0Fu) << 4);
+      const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (Bw & 0xF0F0F0F0u);
+      sts128(row0 + off, e2m1_scaled8(wg, sh0));
+      sts128(row1 + off, e2m1_scaled8(wg8, sh1));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- decode GEMM A operand
+// bf16x2 codes of elements (0, 1) and (2, 3) of a 4-element group from a word whose
+// bytes hold the group's 4-bit codes in the order (e0, e2, e1, e3), one per low nibble:
+// q - 8 for Q4_0 (the byte 0x43 above a code byte is bf16 128 + q; one bf16x2 subtract
+// of 136), the E2M1 value for MXFP4.  Both are exact in bf16.
+template <int QT>
+__device__ __forceinline__ void decode_plain(uint32_t E, uint32_t& o0, uint32_t& o1) {
+  if (QT == FTMOE_Q4_0) {
+    const uint32_t K = 0x43434343u;
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+    uint32_t t0 = prmt(E, K, 0x4240u), t1 = prmt(E, K, 0x4341u);
+    const __nv_bfloat162 u0 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t0), off);
+    const __nv_bfloat162 u1 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t1), off);
+    o0 = *reinterpret_cast<const uint32_t*>(&u0);
+    o1 = *reinterpret_cast<const uint32_t*>(&u1);
+  } else {
+    const uint32_t TWO126 = 0x7E807E80u;
+    const uint32_t v[2] = {prmt(E, 0u, 0x4240u), prmt(E, 0u, 0x4341u)};  // 0x000c000c pairs
+    uint32_t r[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      // ((c & 7) << 6) | ((c & 8) << 12) read as bf16 is E2M1(c) * 2^-126 (the E2M1
+      // subnormal lands on a bf16 subnormal); one bf16 multiply by 2^126 makes it exact
+      uint32_t t = ((v[p] & 0x00070007u) << 6) | ((v[p] & 0x00080008u) << 12);
+      const __nv_bfloat162 w = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&TWO126));
+      r[p] = *reinterpret_cast<const uint32_t*>(&w);
+    }
+    o0 = r[0];
+    o1 = r[1];
+  }
+}
+
+}  // namespace ftmoe

@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "NO_S
 Q4_0, MXFP4 = 1, 2
 QTYPES = {"q4_0": Q4_0, "mxfp4": MXFP4}
 PATH_AUTO, PATH_GEMV, PATH_GEMM, PATH_GEMM_DECODE = 0, 1, 2, 3
+OPERAND_PREFILL, OPERAND_CODES = 0, 1
 LRU_PER_LAYER, LRU_GLOBAL = 0, 1
 
 
@@ -64,6 +65,7 @@ _SIGS = {
     "ftmoe_tiled_bytes": (_sz, [_i, _i, _i, _i]),
     "ftmoe_repack": (_i, [_i, _vp, _vp, _i, _i, _i, _vp]),
     "ftmoe_dequant": (_i, [_i, _vp, _i, _i, _i, _vp, _vp]),
+    "ftmoe_dequant_operand": (_i, [_i, _i, _vp, _i, _i, _i, _vp, _vp]),
     "ftmoe_route": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "ftmoe_permute_workspace_bytes": (_sz, [_i, _i, _i]),
     "ftmoe_permute": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -136,6 +138,11 @@ def ftmoe_repack(qtype, canon, tiles, E, N, K, stream=None):
 
 def ftmoe_dequant(qtype, tiles, E, N, K, out, stream=None):
     _check("ftmoe_dequant", lib.ftmoe_dequant(_qt(qtype), _p(tiles), E, N, K, _p(out), _s(stream)))
+
+
+def ftmoe_dequant_operand(qtype, which, tiles, E, N, K, out, stream=None):
+    _check("ftmoe_dequant_operand", lib.ftmoe_dequant_operand(_qt(qtype), int(which), _p(tiles), E, N, K,
+                                                              _p(out), _s(stream)))
 
 
 def ftmoe_route(logits, T, E, k, ids, w, stream=None):

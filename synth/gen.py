@@ -250,8 +250,11 @@ def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
     """Canonical block bytes uint8 [E, N, K/32, block] of N(0, std) weights.
 
     Expert e draws from its own stream (seed, tag, e).  With ``distinct`` < E only that
-    many expert matrices are drawn and expert e holds a copy of matrix e % distinct
-    (used for the largest banks, where drawing every expert would dominate run time)."""
+    many expert matrices are drawn (used for the largest banks, where drawing every
+    expert would dominate run time); expert e then holds draw src[e] with its rows in a
+    seeded order of its own, where src is a seeded permutation of the experts taken
+    modulo ``distinct``.  Rows of a draw are independent N(0, std) rows, so every expert
+    keeps the distribution, and no two experts hold the same matrix."""
     enc = _ENCODERS[qtype]
     nb = QTYPE_BLOCK_BYTES[qtype]
     out = np.empty((E, N, K // BLOCK, nb), dtype=np.uint8)
@@ -264,8 +267,16 @@ def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
 
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(one, range(D)))
-    for e in range(D, E):
-        out[e] = out[e % D]
+    if D < E:
+        draws = out[:D].copy()
+        src = _rng(seed, tag, "expert_src", E, D).permutation(E) % D
+
+        def place(e):
+            rows = _rng(seed, tag, "expert_rows", e, N).permutation(N)
+            out[e] = draws[src[e]][rows]
+
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(place, range(E)))
     return out
 
 

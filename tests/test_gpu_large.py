@@ -1,8 +1,10 @@
 """Large MoE layer (hidden 7168, expert intermediate 2048, 256 routed experts top-8 plus an
-always-on shared expert, MXFP4, Zipf-skewed routing): one 2048-token prefill chunk (the
-tensor-core path) and a 32-token decode step (the grouped-GEMV path), each checked on
-sampled tokens against the fp64 oracle.  The 256 experts hold copies of 8 distinct
-weight draws so that generating the 6 GB bank stays within a test's time."""
+always-on shared expert, MXFP4, Zipf-skewed routing): a 16384-token prefill run as eight
+2048-token chunks (the tensor-core path) and a 32-token decode step, each checked on
+sampled tokens of every chunk against the fp64 oracle.  The 256 experts are made from 64
+independent weight draws, each expert holding a draw (picked through a seeded
+permutation) with its rows in a seeded order of its own, so that no two experts share a
+matrix and generating the 6 GB bank stays within a test's time."""
 import numpy as np
 import pytest
 
@@ -12,6 +14,7 @@ from tests._util import bf16_tensor, bf16_to_f64, ensure_built, rel_l2
 
 pytestmark = pytest.mark.gpu
 LAYER_TOL = 1e-2
+DRAWS = 64
 
 
 @pytest.fixture(scope="module")
@@ -20,30 +23,51 @@ def large(cuda_device):
     import torch
     from quantized_expert_ffn_layer_b300 import MoELayer
     c = dict(CONFIGS["large"])
-    L = make_layer(**c, distinct=8)
+    L = make_layer(**c, distinct=DRAWS)
     m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=cuda_device)
     yield L, m, torch, cuda_device
     del m
     torch.cuda.empty_cache()
 
 
-def _run_and_check(L, m, torch, dev, x_bits, logits, nrows, seed):
+def test_large_experts_are_all_distinct(large):
+    L = large[0]
+    sig = {bytes(L.w13[e, :2, :2].reshape(-1)) + bytes(L.w2[e, :2, :2].reshape(-1)) for e in range(L.E)}
+    assert len(sig) == L.E
+
+
+def _run(L, m, torch, dev, x_bits, logits):
     T = x_bits.shape[0]
     ids = torch.empty((T, L.k), dtype=torch.int32, device=dev)
     out = m.forward(torch.from_numpy(logits).to(dev), bf16_tensor(x_bits, dev), L.k, ids_out=ids)
     torch.cuda.synchronize()
-    got = bf16_to_f64(out)
-    rows = np.random.default_rng(seed).choice(T, size=nrows, replace=False)
-    rids, _, rout = oracle.layer_rows(x_bits, logits, L.k, L.qtype, L.w13, L.w2, rows,
-                                      L.shared_w13, L.shared_w2)
-    assert np.array_equal(ids.cpu().numpy()[rows], rids)
-    err = rel_l2(got[rows], rout)
-    assert err <= LAYER_TOL, err
+    return bf16_to_f64(out), ids.cpu().numpy()
 
 
-def test_large_prefill_chunk_sampled(large):
+def test_large_prefill_all_chunks_sampled(large):
+    """Every chunk of the 16384-token prefill through the layer; 2 sampled tokens per chunk
+    (16 in all, their experts spread over the bank) against the per-token oracle."""
     L, m, torch, dev = large
-    _run_and_check(L, m, torch, dev, L.x, L.logits, 8, 3)
+    c = CONFIGS["large"]
+    nchunks = c["T_total"] // c["T"]
+    xs, lgs, gots, ids_all = [], [], [], []
+    for ci in range(nchunks):
+        x = L.x if ci == 0 else gen_x_bf16(0, c["T"], L.H, f"x_chunk{ci}")
+        lg = L.logits if ci == 0 else gen_logits(0, c["T"], L.E, zipf=1.0, tag=f"logits_chunk{ci}")
+        got, ids = _run(L, m, torch, dev, x, lg)
+        rows = np.random.default_rng(100 + ci).choice(c["T"], size=2, replace=False)
+        xs.append(x[rows])
+        lgs.append(lg[rows])
+        gots.append(got[rows])
+        ids_all.append(ids[rows])
+    x = np.concatenate(xs)
+    lg = np.concatenate(lgs)
+    rids, _, rout = oracle.layer_rows(x, lg, L.k, L.qtype, L.w13, L.w2, np.arange(len(x)),
+                                      L.shared_w13, L.shared_w2)
+    assert np.array_equal(np.concatenate(ids_all), rids)
+    assert len(np.unique(rids)) >= 32  # the sample reaches many experts, not a few hot ones
+    err = rel_l2(np.concatenate(gots), rout)
+    assert err <= LAYER_TOL, err
 
 
 def test_large_decode_step_sampled(large):
@@ -51,4 +75,8 @@ def test_large_decode_step_sampled(large):
     T = CONFIGS["large"]["decode_T"]
     x = gen_x_bf16(0, T, L.H, "decode_x")
     lg = gen_logits(0, T, L.E, zipf=1.0, tag="decode_logits")
-    _run_and_check(L, m, torch, dev, x, lg, 8, 4)
+    got, ids = _run(L, m, torch, dev, x, lg)
+    rows = np.random.default_rng(4).choice(T, size=8, replace=False)
+    rids, _, rout = oracle.layer_rows(x, lg, L.k, L.qtype, L.w13, L.w2, rows, L.shared_w13, L.shared_w2)
+    assert np.array_equal(ids[rows], rids)
+    assert rel_l2(got[rows], rout) <= LAYER_TOL

@@ -20,8 +20,9 @@ struct ftmoe_cache {
   std::vector<uint64_t> stamp;
   std::vector<cudaEvent_t> copy_done, busy;
   std::vector<char> copy_unwaited, has_busy;
+  std::vector<int> pins;                       // per global slot: acquires not yet released
   std::unordered_map<long long, int> where;   // (layer * E + e) -> global slot
-  std::vector<std::vector<int>> last_acquired;  // per layer: global slots of the last acquire
+  std::vector<std::vector<int>> pinned;        // per layer: slots its acquires pinned
   std::vector<std::vector<int32_t>> last_ids;   // per layer: expert ids of the last acquire
   std::vector<cudaEvent_t> layer_done;          // per layer, recorded at release
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timing_pending;
@@ -48,8 +49,11 @@ cudaEvent_t timing_event(ftmoe_cache* c) {
 }
 
 // Touches ids in order (see ftmoe.h); issues the copies of misses on the copy stream.
+// All or nothing: the slot of every id is planned first, and a request that finds no
+// slot for a missing id returns FTMOE_ERR_NO_SLOT before any record changes.  With
+// `pin` (an acquire) the touched slots stay pinned until the layer's release.
 ftmoe_status request(ftmoe_cache* c, int layer, const int32_t* ids, int n, int32_t* slots_out,
-                     uint8_t* copied_out, std::vector<int>* gslots, int* ncopies) {
+                     uint8_t* copied_out, std::vector<int>* gslots, int* ncopies, bool pin) {
   if (layer < 0 || layer >= c->d.layers || n < 0 || (n > 0 && !ids)) return FTMOE_ERR_INVALID_ARG;
   for (int i = 0; i < n; ++i)
     if (ids[i] < 0 || ids[i] >= c->d.E) return FTMOE_ERR_INVALID_ARG;
@@ -57,43 +61,69 @@ ftmoe_status request(ftmoe_cache* c, int layer, const int32_t* ids, int n, int32
   const int pool = pool_of(c, layer);
   const int base = pool * c->nslot;
   cudaStream_t cs = (cudaStream_t)c->d.copy_stream;
-  std::vector<char> touched(c->nslot, 0);
+  // ---- plan (no record changes): a slot taken for a miss is touched, so it is taken at
+  // most once per request, and the stamps of untouched slots do not change meanwhile
+  std::vector<char> touched(c->nslot, 0), retaken(c->nslot, 0);
+  std::unordered_map<long long, int> taken;  // keys placed by this request -> pool slot
+  std::vector<int> plan_slot(n);
+  std::vector<char> plan_copy(n);
+  for (int i = 0; i < n; ++i) {
+    const long long key = (long long)layer * c->d.E + ids[i];
+    int s = -1;
+    auto tk = taken.find(key);
+    if (tk != taken.end()) {
+      s = tk->second;
+    } else {
+      auto it = c->where.find(key);
+      if (it != c->where.end() && !retaken[it->second - base]) s = it->second - base;
+    }
+    const bool copied = s < 0;
+    if (copied) {
+      for (int q = 0; q < c->nslot && s < 0; ++q)
+        if (!touched[q] && !c->pins[base + q] && c->owner_layer[base + q] < 0) s = q;
+      if (s < 0) {
+        uint64_t best = UINT64_MAX;
+        for (int q = 0; q < c->nslot; ++q)
+          if (!touched[q] && !c->pins[base + q] && c->stamp[base + q] < best) {
+            best = c->stamp[base + q];
+            s = q;
+          }
+      }
+      if (s < 0) return FTMOE_ERR_NO_SLOT;
+      retaken[s] = 1;
+      taken[key] = s;
+    }
+    touched[s] = 1;
+    plan_slot[i] = s;
+    plan_copy[i] = copied ? 1 : 0;
+  }
+  // ---- commit
   std::vector<int> to_copy;  // global slots whose blob must be copied
   std::vector<long long> to_copy_key;
   for (int i = 0; i < n; ++i) {
     const long long key = (long long)layer * c->d.E + ids[i];
+    const int s = plan_slot[i], gs = base + s;
     ++c->clock;
-    int s;
-    bool copied = false;
-    auto it = c->where.find(key);
-    if (it != c->where.end()) {
-      s = it->second - base;
-    } else {
-      int victim = -1;
-      for (int q = 0; q < c->nslot && victim < 0; ++q)
-        if (!touched[q] && c->owner_layer[base + q] < 0) victim = q;
-      if (victim < 0) {
-        uint64_t best = UINT64_MAX;
-        for (int q = 0; q < c->nslot; ++q)
-          if (!touched[q] && c->stamp[base + q] < best) { best = c->stamp[base + q]; victim = q; }
-      }
-      s = victim;
-      const int gs = base + s;
+    if (plan_copy[i]) {
       if (c->owner_layer[gs] >= 0)
         c->where.erase((long long)c->owner_layer[gs] * c->d.E + c->owner_expert[gs]);
       c->owner_layer[gs] = layer;
       c->owner_expert[gs] = ids[i];
       c->where[key] = gs;
-      copied = true;
       to_copy.push_back(gs);
       to_copy_key.push_back(key);
     }
-    c->stamp[base + s] = c->clock;
-    touched[s] = 1;
+    c->stamp[gs] = c->clock;
     if (slots_out) slots_out[i] = s;
-    if (copied_out) copied_out[i] = copied ? 1 : 0;
-    if (gslots) gslots->push_back(base + s);
+    if (copied_out) copied_out[i] = plan_copy[i];
+    if (gslots) gslots->push_back(gs);
   }
+  if (pin)
+    for (int q = 0; q < c->nslot; ++q)
+      if (touched[q]) {
+        ++c->pins[base + q];
+        c->pinned[layer].push_back(base + q);
+      }
   *ncopies = (int)to_copy.size();
   if (to_copy.empty()) return FTMOE_OK;
   // a victim slot may still be read by compute work released on it: wait for that first
@@ -146,7 +176,8 @@ ftmoe_status ftmoe_cache_create(const ftmoe_cache_desc* d, ftmoe_cache** out) {
   c->busy.assign(total, nullptr);
   c->copy_unwaited.assign(total, 0);
   c->has_busy.assign(total, 0);
-  c->last_acquired.resize(d->layers);
+  c->pins.assign(total, 0);
+  c->pinned.resize(d->layers);
   c->last_ids.resize(d->layers);
   c->layer_done.assign(d->layers, nullptr);
   bool ok = true;
@@ -167,7 +198,7 @@ ftmoe_status ftmoe_cache_prefetch(ftmoe_cache* c, int layer, const int32_t* ids,
                                   int32_t* slots_out, uint8_t* copied_out) {
   if (!c) return FTMOE_ERR_INVALID_ARG;
   int nc = 0;
-  ftmoe_status s = request(c, layer, ids, n, slots_out, copied_out, nullptr, &nc);
+  ftmoe_status s = request(c, layer, ids, n, slots_out, copied_out, nullptr, &nc, false);
   if (s == FTMOE_OK) {
     c->st.prefetch_lookups += (uint64_t)n;
     c->st.prefetch_copies += (uint64_t)nc;
@@ -181,7 +212,7 @@ ftmoe_status ftmoe_cache_acquire(ftmoe_cache* c, int layer, const int32_t* ids, 
   if (!c || !blob_out) return FTMOE_ERR_INVALID_ARG;
   std::vector<int> gs;
   int nc = 0;
-  ftmoe_status s = request(c, layer, ids, n, slots_out, copied_out, &gs, &nc);
+  ftmoe_status s = request(c, layer, ids, n, slots_out, copied_out, &gs, &nc, true);
   if (s != FTMOE_OK) return s;
   c->st.lookups += (uint64_t)n;
   c->st.misses += (uint64_t)nc;
@@ -195,7 +226,6 @@ ftmoe_status ftmoe_cache_acquire(ftmoe_cache* c, int layer, const int32_t* ids, 
     }
     blob_out[ids[i]] = (const char*)c->d.pool + (size_t)g * c->d.blob_bytes;
   }
-  c->last_acquired[layer] = gs;
   c->last_ids[layer].assign(ids, ids + n);
   return FTMOE_OK;
 }
@@ -218,10 +248,12 @@ ftmoe_status ftmoe_cache_release(ftmoe_cache* c, int layer, ftmoe_stream_t compu
   if (!c || layer < 0 || layer >= c->d.layers) return FTMOE_ERR_INVALID_ARG;
   cudaEvent_t ev = c->layer_done[layer];
   if (cudaEventRecord(ev, (cudaStream_t)compute) != cudaSuccess) return FTMOE_ERR_CUDA;
-  for (int g : c->last_acquired[layer]) {
+  for (int g : c->pinned[layer]) {
     c->busy[g] = ev;
     c->has_busy[g] = 1;
+    --c->pins[g];
   }
+  c->pinned[layer].clear();
   return FTMOE_OK;
 }
 

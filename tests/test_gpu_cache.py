@@ -59,15 +59,15 @@ def test_cache_matches_lru_simulator_and_contiguous_layer(env, policy):
     for st in range(steps):
         # prefetch layer 0 of the step, then per layer: prefetch the next, acquire this one
         pslots, pcopied = cache.prefetch(0, trace[st, 0])
-        want = sim.request(0, trace[st, 0])
+        want = sim.prefetch(0, trace[st, 0])
         assert [s for s, _ in want] == pslots and [c for _, c in want] == pcopied
         for l in range(LAYERS):
             if l + 1 < LAYERS:
                 pslots, pcopied = cache.prefetch(l + 1, trace[st, l + 1])
-                want = sim.request(l + 1, trace[st, l + 1])
+                want = sim.prefetch(l + 1, trace[st, l + 1])
                 assert [s for s, _ in want] == pslots and [c for _, c in want] == pcopied
             blob_ptrs, slots, copied = cache.acquire(l, trace[st, l], compute)
-            want = sim.request(l, trace[st, l])
+            want = sim.acquire(l, trace[st, l])
             assert [s for s, _ in want] == slots and [c for _, c in want] == copied
             misses += sum(copied)
             hits += len(copied) - sum(copied)
@@ -84,6 +84,7 @@ def test_cache_matches_lru_simulator_and_contiguous_layer(env, policy):
             out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
             F.ftmoe_layer(wt, lg, x, 1, K, out, None, None, ws, ws.numel())
             cache.release(l, compute)
+            sim.release(l)
             ref = m.forward(lg, x, K)
             torch.cuda.synchronize()
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (st, l)
@@ -136,17 +137,75 @@ def test_history_prefetch_matches_simulator(env, policy):
             ids, slots, copied = cache.prefetch_history(nxt)
             assert ids == last.get(nxt, [])
             if ids:
-                want = sim.request(nxt, ids)
+                want = sim.prefetch(nxt, ids)
                 assert [s for s, _ in want] == slots and [c for _, c in want] == copied
             _, slots, copied = cache.acquire(l, trace[st, l], compute)
-            want = sim.request(l, trace[st, l])
+            want = sim.acquire(l, trace[st, l])
             assert [s for s, _ in want] == slots and [c for _, c in want] == copied
             last[l] = [int(v) for v in trace[st, l]]
             cache.release(l, compute)
+            sim.release(l)
     torch.cuda.synchronize()
     pool_h = pool.view(-1, nb).cpu()
     nslot = SLOTS if policy == "layer" else SLOTS * LAYERS
     for (l, e), s in sim.where.items():
         gs = (l * nslot + s) if policy == "layer" else s
         assert torch.equal(pool_h[gs], bank[l, e]), (l, e, s)
+    cache.close()
+
+
+def test_acquired_slots_are_not_overwritten_before_release(env):
+    """A global pool of E + 2 slots (less than two layers of experts): layer 0 acquires
+    all E experts and, before it runs, layer 1's prefetch of all E is refused with
+    NO_SLOT instead of overwriting slots layer 0 is about to read; a prefetch that fits
+    the two unpinned slots succeeds.  Layer 0 computed from its slots equals the layer
+    from contiguous weights bit for bit; after the release, layer 1 is fetched, acquired
+    and checked the same way.  Every slot choice equals the simulator's."""
+    F, torch, dev = env
+    layers, bank, nb = _bank(env, "q4_0")
+    nl = 2
+    pool = torch.zeros((E + 2) * nb, dtype=torch.uint8, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    compute = torch.cuda.current_stream(dev)
+    # slots_per_layer * layers = E + 2 slots in the one global pool
+    cache = F.ExpertCache(nl, E, nb, bank, pool, (E + 2) // nl,
+                          F.LRU_GLOBAL, copy_stream)
+    sim = oracle.LRUSim(nl, E, (E + 2) // nl, "global")
+    everyone = list(range(E))
+
+    def run_from_slots(l, blob_ptrs):
+        L, m, _ = layers[l]
+        lg = torch.from_numpy(np.random.default_rng(l).standard_normal((16, E)).astype(np.float32)).to(dev)
+        x = bf16_tensor(np.repeat(L.x, 16, axis=0), dev)
+        wt = F.make_weights("q4_0", E, H, I, expert_blob=blob_ptrs)
+        ws = m.workspace(16, K)
+        out = torch.empty((16, H), dtype=torch.bfloat16, device=dev)
+        F.ftmoe_layer(wt, lg, x, 16, K, out, None, None, ws, ws.numel())
+        return out, m.forward(lg, x, K)
+
+    blobs, slots, copied = cache.acquire(0, everyone, compute)
+    assert [(s, c) for s, c in zip(slots, copied)] == sim.acquire(0, everyone)
+    with pytest.raises(F.FtmoeError) as ei:
+        cache.prefetch(1, everyone)
+    assert ei.value.status == 4  # FTMOE_ERR_NO_SLOT
+    with pytest.raises(oracle.cache.NoSlot):
+        sim.prefetch(1, everyone)
+    pslots, pcopied = cache.prefetch(1, [3, 5])
+    assert list(zip(pslots, pcopied)) == sim.prefetch(1, [3, 5])
+    out, ref = run_from_slots(0, blobs)
+    cache.release(0, compute)
+    sim.release(0)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    pslots, pcopied = cache.prefetch(1, everyone)
+    assert list(zip(pslots, pcopied)) == sim.prefetch(1, everyone)
+    blobs, slots, copied = cache.acquire(1, everyone, compute)
+    assert list(zip(slots, copied)) == sim.acquire(1, everyone)
+    out, ref = run_from_slots(1, blobs)
+    cache.release(1, compute)
+    sim.release(1)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    st = cache.stats()
+    assert st["h2d_bytes"] == nb * (st["misses"] + st["prefetch_copies"])
     cache.close()

@@ -80,3 +80,36 @@ def test_misses_equal_a_textbook_lru(policy):
     got = [copied for layer, ids in trace for _, copied in sim.request(layer, ids)]
     cap = slots if policy == "layer" else slots * layers
     assert got == _textbook_lru_misses(trace, cap, policy == "global")
+
+
+def test_acquired_slots_are_pinned_until_release():
+    """A layer's acquired slots cannot be taken by a later request until the layer is
+    released: a prefetch that would need them fails with NoSlot and changes nothing."""
+    c = LRUSim(layers=2, E=8, slots_per_layer=3, policy="global")  # 6 slots
+    assert c.acquire(0, [0, 1, 2, 3]) == [(0, True), (1, True), (2, True), (3, True)]
+    before = (list(c.owner[0]), list(c.stamp[0]), dict(c.where), c.clock)
+    with pytest.raises(NoSlot):
+        c.prefetch(1, [4, 5, 6])          # 3 misses, only slots 4 and 5 unpinned
+    assert (list(c.owner[0]), list(c.stamp[0]), dict(c.where), c.clock) == before
+    assert c.prefetch(1, [4, 5]) == [(4, True), (5, True)]
+    with pytest.raises(NoSlot):
+        c.prefetch(1, [4, 5, 6])          # 4, 5 touched by this request, 0..3 pinned
+    c.release(0)
+    assert c.prefetch(1, [6]) == [(0, True)]  # slot 0 is now the least recently used
+    assert c.acquire(0, [1]) == [(1, False)]
+
+
+def test_pins_count_every_acquire_until_release():
+    c = LRUSim(layers=1, E=8, slots_per_layer=2)
+    c.acquire(0, [0])
+    c.acquire(0, [0, 1])                  # slot 0 pinned twice, slot 1 once
+    with pytest.raises(NoSlot):
+        c.prefetch(0, [2])
+    c.release(0)                          # releases both acquires
+    assert c.prefetch(0, [2]) == [(0, True)]
+
+
+def test_prefetch_pins_nothing():
+    c = LRUSim(layers=1, E=8, slots_per_layer=2)
+    c.prefetch(0, [0, 1])
+    assert c.prefetch(0, [2, 3]) == [(0, True), (1, True)]

@@ -65,8 +65,11 @@ typedef enum {
 
 /* Block formats ([P5] §五 bank schemas).  Q4_0: 32 weights per block, fp16
  * scale d, weight = (q - 8) * d.  MXFP4: 32 E2M1 codes sharing an E8M0 scale
- * 2^(e - 127) (e = 255 is NaN). */
-typedef enum { FTMOE_Q4_0 = 1, FTMOE_MXFP4 = 2 } ftmoe_qtype;
+ * 2^(e - 127) (e = 255 is NaN).  NVFP4: 16 E2M1 codes sharing an E4M3 scale s,
+ * and one fp32 tensor scale t per expert matrix: weight = E2M1 * s * t.  MXFP8
+ * (the block-scaled FP8 bank; OCP MX v1.0): 32 E4M3 elements sharing an E8M0
+ * scale 2^(e - 127). */
+typedef enum { FTMOE_Q4_0 = 1, FTMOE_MXFP4 = 2, FTMOE_NVFP4 = 3, FTMOE_MXFP8 = 4 } ftmoe_qtype;
 
 /* Expert FFN path selection (ftmoe_set_ffn_path). */
 typedef enum {
@@ -91,13 +94,23 @@ int ftmoe_version(void);
  * MXFP4 block).  Expert e's gate/up matrix w13[e] is [2I][H] (rows [0, I)
  * gate, [I, 2I) up); its down matrix w2[e] is [H][I].
  *
+ * MXFP8 blocks hold 32 weights in 33 bytes (E8M0 scale, then the 32 E4M3
+ * element bytes in order).
+ * NVFP4 blocks hold 16 weights in 9 bytes (E4M3 scale, then 8 code bytes:
+ * element i < 8 in the low nibble of code byte i, i >= 8 in the high nibble of
+ * byte i - 8), and the canonical buffer ends with the E fp32 tensor scales
+ * (little-endian): E * N * (K / 16) * 9 + 4 E bytes.
+ *
  * The kernels read a tiled layout instead ("tiles"): for each expert and
  * each group of 16 rows, ceil(K / 64) records of 64 reduction elements; a
- * record is 512 code bytes followed by the 32 block scales of its 16 rows x 2
- * blocks (64 bytes of fp16 for Q4_0, 32 bytes of E8M0 for MXFP4), so records
- * are 576 / 544 bytes and every record starts 16-byte aligned.  A ragged last
- * record (K % 64 == 32) is padded with zero weights.  N must be a multiple
- * of 16.
+ * record is 512 code bytes (1024 element bytes for MXFP8) followed by the
+ * block scales of its 16 rows (64 bytes of fp16 for Q4_0 and 32 bytes of E8M0
+ * for MXFP4 and MXFP8, 2 blocks per row; 64 E4M3 bytes for NVFP4, 4 blocks per
+ * row), so records are 576 / 544 / 576 / 1056 bytes and every record starts
+ * 16-byte aligned.  For NVFP4 each expert's
+ * records are followed by a 16-byte trailer holding its tensor scale.  A ragged
+ * last record (K % 64 == 32) is padded with zero weights.  N must be a
+ * multiple of 16.
  */
 
 /* Bytes of the tiled layout of W[E][N][K]; 0 for invalid arguments. */
@@ -125,7 +138,9 @@ typedef enum {
                                 ((q - 8) * d for Q4_0, E2M1 * 2^(e - 127) for MXFP4);
                                 beyond the bf16 range -> +-inf; NaN scales -> NaN */
   FTMOE_OPERAND_CODES = 1    /* decode GEMM A operand: the unscaled code value, q - 8
-                                (Q4_0) or the E2M1 value (MXFP4), exact */
+                                (Q4_0) or the E2M1 value (MXFP4, NVFP4), exact; for MXFP8
+                                the grouped GEMV's: the E4M3 element value, exact for
+                                every finite code (the NaN code reads as +-480) */
 } ftmoe_operand;
 
 /* Writes operand `which` of tiles (device) as bf16 bit patterns out[E][N][K] (device,

@@ -114,9 +114,14 @@ def decode_mxfp8(blocks: np.ndarray) -> np.ndarray:
     return w.reshape(*blocks.shape[:-2], blocks.shape[-2] * BLOCK)
 
 
-def decode_blocks(blocks: np.ndarray, qtype: str) -> np.ndarray:
+def decode_blocks(blocks: np.ndarray, qtype: str, tensor_scale=None) -> np.ndarray:
+    """Blocks of one format -> fp64 weights; NVFP4 also takes its matrix's tensor scale."""
     if qtype == "q4_0":
         return decode_q4_0(blocks)
     if qtype == "mxfp4":
         return decode_mxfp4(blocks)
+    if qtype == "nvfp4":
+        return decode_nvfp4(blocks, tensor_scale)
+    if qtype == "mxfp8":
+        return decode_mxfp8(blocks)
     raise ValueError(f"unknown qtype {qtype!r}")

@@ -20,27 +20,35 @@ def _x_fp64(x_bf16_bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
-def layer(x_bits, logits, k, qtype, w13, w2, shared_w13=None, shared_w2=None):
+def _dec(blocks, qtype, ts, name, e):
+    """Expert e's matrix `name` decoded; ts (NVFP4: {name: float32 [E]}) gives its tensor scale."""
+    return decode_blocks(blocks[e], qtype, None if ts is None else ts[name][e])
+
+
+def layer(x_bits, logits, k, qtype, w13, w2, shared_w13=None, shared_w2=None, ts=None):
     """Full layer on all tokens.
 
-    x_bits uint16 bf16 [T, H]; logits float32 [T, E]; w13 uint8 [E, 2I, H/32, blk];
-    w2 uint8 [E, H, I/32, blk].  Returns a dict with ids, w, offsets, sorted_pair,
-    inv_pos, y_perm [P, H] and out [T, H] (fp64)."""
+    x_bits uint16 bf16 [T, H]; logits float32 [T, E]; w13 uint8 [E, 2I, H/bs, blk];
+    w2 uint8 [E, H, I/bs, blk]; ts: NVFP4's per-matrix tensor scales
+    {"w13": [E], "w2": [E], "shared_w13": [1], "shared_w2": [1]} (None otherwise).
+    Returns a dict with ids, w, offsets, sorted_pair, inv_pos, y_perm [P, H] and
+    out [T, H] (fp64)."""
     x = _x_fp64(x_bits)
     E = w13.shape[0]
     ids, w = route(logits, k)
     offsets, sorted_pair, inv_pos = permute(ids, E)
     y = expert_ffn(x, k, offsets, sorted_pair,
-                   lambda e: decode_blocks(w13[e], qtype), lambda e: decode_blocks(w2[e], qtype))
+                   lambda e: _dec(w13, qtype, ts, "w13", e), lambda e: _dec(w2, qtype, ts, "w2", e))
     sh = None
     if shared_w13 is not None:
-        sh = swiglu_ffn(x, decode_blocks(shared_w13[0], qtype), decode_blocks(shared_w2[0], qtype))
+        sh = swiglu_ffn(x, _dec(shared_w13, qtype, ts, "shared_w13", 0),
+                        _dec(shared_w2, qtype, ts, "shared_w2", 0))
     out = combine(y, w, inv_pos, sh)
     return dict(ids=ids, w=w, offsets=offsets, sorted_pair=sorted_pair, inv_pos=inv_pos,
                 y_perm=y, out=out, shared_y=sh)
 
 
-def layer_rows(x_bits, logits, k, qtype, w13, w2, rows, shared_w13=None, shared_w2=None):
+def layer_rows(x_bits, logits, k, qtype, w13, w2, rows, shared_w13=None, shared_w2=None, ts=None):
     """Layer output for a subset of tokens, by the per-token definition.
 
     A token's output depends only on its own activations and logits:
@@ -55,9 +63,10 @@ def layer_rows(x_bits, logits, k, qtype, w13, w2, rows, shared_w13=None, shared_
     out = np.zeros((n, H))
     for e in np.unique(ids):
         sel_i, sel_j = np.nonzero(ids == e)
-        y = swiglu_ffn(x[sel_i], decode_blocks(w13[e], qtype), decode_blocks(w2[e], qtype))
+        y = swiglu_ffn(x[sel_i], _dec(w13, qtype, ts, "w13", e), _dec(w2, qtype, ts, "w2", e))
         for r, (i, j) in enumerate(zip(sel_i, sel_j)):
             out[i] += w[i, j] * y[r]
     if shared_w13 is not None:
-        out += swiglu_ffn(x, decode_blocks(shared_w13[0], qtype), decode_blocks(shared_w2[0], qtype))
+        out += swiglu_ffn(x, _dec(shared_w13, qtype, ts, "shared_w13", 0),
+                          _dec(shared_w2, qtype, ts, "shared_w2", 0))
     return ids, w, out

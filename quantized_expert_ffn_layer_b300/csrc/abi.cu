@@ -32,7 +32,7 @@ ftmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FTMOE_OK : FTM
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-bool qtype_ok(int q) { return q == FTMOE_Q4_0 || q == FTMOE_MXFP4; }
+bool qtype_ok(int q) { return q >= FTMOE_Q4_0 && q <= FTMOE_MXFP8; }
 bool dim_ok(int v) { return v > 0 && v <= 16384 && v % 32 == 0; }
 bool tke_ok(int T, int k, int E) {
   return T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32 &&
@@ -127,7 +127,8 @@ ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, 
     if (e != cudaErrorNotSupported) return FTMOE_ERR_CUDA;
     if (path == FTMOE_PATH_GEMM_DECODE) return FTMOE_ERR_UNSUPPORTED;
   }
-  return from_cuda(launch_ffn_gemv(pb, fw.gemv_ws, ws_zeroed, st));
+  const cudaError_t e = launch_ffn_gemv(pb, fw.gemv_ws, ws_zeroed, st);
+  return e == cudaErrorNotSupported ? FTMOE_ERR_UNSUPPORTED : from_cuda(e);
 }
 }  // namespace
 

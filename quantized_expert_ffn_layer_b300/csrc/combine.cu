@@ -11,7 +11,7 @@ constexpr int COMBINE_THREADS = 128;
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(
     const uint16_t* __restrict__ y_perm, const float* __restrict__ w,
     const int32_t* __restrict__ inv_pos, const uint16_t* __restrict__ shared_y, int T, int k, int H,
-    uint16_t* __restrict__ out) {
+    uint16_t* __restrict__ out, int* status) {
   const int t = blockIdx.x;
   const int col = (blockIdx.y * COMBINE_THREADS + threadIdx.x) * 8;
   if (col >= H) return;
@@ -21,6 +21,12 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(
   for (int j = 0; j < k; ++j) {
     const int r = inv_pos[(size_t)t * k + j];
     if (r < 0) continue;
+#if FTMOE_CHECKS
+    if (r >= T * k) {
+      set_device_code(status, DEV_BAD_INDEX);
+      continue;
+    }
+#endif
     const float wj = w[(size_t)t * k + j];
     const uint4 v = *reinterpret_cast<const uint4*>(y_perm + (size_t)r * H + col);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -50,7 +56,9 @@ cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t
                            const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
                            cudaStream_t st) {
   const dim3 grid(T, (H / 8 + COMBINE_THREADS - 1) / COMBINE_THREADS);
-  combine_kernel<<<grid, COMBINE_THREADS, 0, st>>>(y_perm, w, inv_pos, shared_y, T, k, H, out);
+  const DeviceInfo* di = device_info();
+  combine_kernel<<<grid, COMBINE_THREADS, 0, st>>>(y_perm, w, inv_pos, shared_y, T, k, H, out,
+                                                    di ? di->status : nullptr);
   return cudaGetLastError();
 }
 

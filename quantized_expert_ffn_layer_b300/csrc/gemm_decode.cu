@@ -119,7 +119,7 @@ constexpr size_t gd_smem_bytes() {
 struct GemmArgs {
   const int32_t* offsets;
   const int32_t* sorted_pair;  // gate/up: pair of each permuted row (nullptr: identity)
-  int k, E;
+  int k, E, T, P;
   const uint16_t* act;  // gate/up: x [T][H] (rows gathered); down: h [P][I] (contiguous rows)
   int act_ld;
   uint16_t* out;        // gate/up: h [P][I]; down: y_perm [P][H]
@@ -161,7 +161,8 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   GmItem it;
   it.e = lo;
   const int local = i - citem[lo];
-  const int beg = a.offsets[lo], ne = a.offsets[lo + 1] - beg;
+  int beg, ne;
+  expert_rows(a.offsets, lo, a.P, nullptr, beg, ne);  // (reported by the item count)
   const int ntt = (ne + GD_TOK - 1) / GD_TOK;
   const int ft = local / ntt, tt = local - ft * ntt;
   it.r0 = beg + tt * GD_TOK;
@@ -275,7 +276,11 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
     for (int e0 = 0; e0 < a.E; e0 += 32) {
       const int e = e0 + lane;
       int v = 0;
-      if (e < a.E) v = ((a.offsets[e + 1] - a.offsets[e] + GD_TOK - 1) / GD_TOK) * a.ft_per_expert;
+      if (e < a.E) {
+        int r0, n;
+        expert_rows(a.offsets, e, a.P, a.status, r0, n);
+        v = ((n + GD_TOK - 1) / GD_TOK) * a.ft_per_expert;
+      }
       int x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(GD_THREADS, 1)
       const GmItem it = gm_item<MODE>(item, a, tl.citem);
       rowp = nullptr;
       if (brow < it.n) {
-        const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + brow] / a.k : (it.r0 + brow);
+        const long long ar = row_token(a.sorted_pair, it.r0 + brow, a.k, a.T, a.status);
         rowp = a.act + ar * a.act_ld + ch * 8;
       }
     };
@@ -587,6 +592,8 @@ static cudaError_t gd_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   a.sorted_pair = pb.sorted_pair;
   a.k = pb.k;
   a.E = pb.E;
+  a.T = pb.T;
+  a.P = pb.P;
   a.status = di->status;
   a.act = pb.x;
   a.act_ld = pb.H;
@@ -622,6 +629,10 @@ static cudaError_t gd_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
 }  // namespace dec
 
 cudaError_t launch_ffn_gemm_decode(const FfnProblem& pb, cudaStream_t st) {
+  // NVFP4's 16-element blocks would need twice the partial-sum stages and MXFP8's records
+  // another converter; the library runs those formats through the grouped GEMV at these
+  // batch sizes instead
+  if (pb.qtype == FTMOE_NVFP4 || pb.qtype == FTMOE_MXFP8) return cudaErrorNotSupported;
   if (pb.E > dec::GD_MAX_E) return cudaErrorNotSupported;
   if (pb.table) {
     dec::GmWithTable t;

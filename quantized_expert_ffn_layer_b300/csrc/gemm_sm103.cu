@@ -60,39 +60,55 @@ constexpr int GM_ECOL = 16;               // accumulator columns (tokens) per ep
 constexpr int GM_STG = GM_ECOL * 64;      // epilogue staging per warp: 16 rows x 32 bf16
 constexpr int GM_MAX_E = 1024;
 
-// Per-projection layout: gate/up stages hold two A tiles, down stages one.
-template <int MODE>
+// Per-projection layout: gate/up stages hold two A tiles, down stages one.  MXFP8's raw
+// records are twice as large, so it trades one operand stage for deeper raw rings.
+// Ring depths (overridable at build time for sweeps): operand stages and raw-record
+// stages of the gate/up (0) and down (1) projections, for the 4-bit formats.
+#ifndef FTMOE_GM_NS0
+#define FTMOE_GM_NS0 3
+#endif
+#ifndef FTMOE_GM_NR0
+#define FTMOE_GM_NR0 2
+#endif
+#ifndef FTMOE_GM_NS1
+#define FTMOE_GM_NS1 4
+#endif
+#ifndef FTMOE_GM_NR1
+#define FTMOE_GM_NR1 4
+#endif
+constexpr int GM_MAX_STAGES = 8;
+template <int QT, int MODE>
 struct GmCfg {
+  static constexpr bool FP8 = QT == FTMOE_MXFP8;
   static constexpr int NT = MODE == 0 ? 2 : 1;           // A tiles (MMAs per k-step)
   static constexpr int NACC = MODE == 0 ? 1 : 2;         // accumulator buffers
-  static constexpr int NS = MODE == 0 ? 3 : 4;           // operand stages
-  static constexpr int NR = MODE == 0 ? 2 : 4;           // raw weight stages
+  static constexpr int NS = MODE == 0 ? (FP8 ? 2 : FTMOE_GM_NS0) : (FP8 ? 3 : FTMOE_GM_NS1);  // operand stages
+  static constexpr int NR = MODE == 0 ? (FP8 ? 3 : FTMOE_GM_NR0) : FTMOE_GM_NR1;              // raw stages
+  static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES, "ring depth");
   static constexpr int NREC = 8 * NT;                    // records per stage
   static constexpr int STAGE = NT * GM_A_TILE + GM_B_TILE;
-  static constexpr int RAW_STAGE = NREC * 576;
-  static constexpr int TPR = GM_CONV_THREADS / NREC;     // converter threads per record
-  static constexpr int NSTEP = 4 * 16 / TPR;              // 16-element steps per thread
+  static constexpr int RAW_STAGE = NREC * rec_bytes(QT);
 };
 
 struct GemmTail {
-  uint64_t a_full[4], b_full[4], empty[4];
-  uint64_t raw_full[4], raw_empty[4];
+  uint64_t a_full[GM_MAX_STAGES], b_full[GM_MAX_STAGES], empty[GM_MAX_STAGES];
+  uint64_t raw_full[GM_MAX_STAGES], raw_empty[GM_MAX_STAGES];
   uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
   int citem[GM_MAX_E + 1];  // exclusive prefix of items per expert
 };
-template <int MODE>
+template <int QT, int MODE>
 constexpr size_t gm_smem_bytes() {
-  return 1024 + (size_t)GmCfg<MODE>::NS * GmCfg<MODE>::STAGE +
-         (size_t)GmCfg<MODE>::NR * GmCfg<MODE>::RAW_STAGE + (size_t)GM_EPI_WARPS * GM_STG +
+  return 1024 + (size_t)GmCfg<QT, MODE>::NS * GmCfg<QT, MODE>::STAGE +
+         (size_t)GmCfg<QT, MODE>::NR * GmCfg<QT, MODE>::RAW_STAGE + (size_t)GM_EPI_WARPS * GM_STG +
          sizeof(GemmTail);
 }
 
 struct GemmArgs {
   const int32_t* offsets;
   const int32_t* sorted_pair;  // gate/up: pair of each permuted row (nullptr: identity)
-  int k, E;
+  int k, E, T, P;
   const uint16_t* act;  // gate/up: x [T][H] (rows gathered); down: h [P][I] (via act_map)
   int act_ld;
   uint16_t* out;        // gate/up: h [P][I]; down: y_perm [P][H]
@@ -105,6 +121,7 @@ struct GemmArgs {
   int nrows;             // output rows of the projection's result: I or H
   int up_row0;           // gate/up: first up row of w13 (= I)
   int ft_per_expert;     // weight-row slices per token tile
+  long long rec_total;   // bytes of one expert's records of this projection (NVFP4 trailer offset)
   int* status;
 };
 
@@ -134,7 +151,8 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   GmItem it;
   it.e = lo;
   const int local = i - citem[lo];
-  const int beg = a.offsets[lo], ne = a.offsets[lo + 1] - beg;
+  int beg, ne;
+  expert_rows(a.offsets, lo, a.P, nullptr, beg, ne);  // (reported by the item count)
   const int ntt = (ne + GM_TOK - 1) / GM_TOK;
   const int ft = local / ntt, tt = local - ft * ntt;
   it.r0 = beg + tt * GM_TOK;
@@ -184,7 +202,7 @@ template <int QT, int MODE, class Tab>
 __global__ void __launch_bounds__(GM_THREADS, 1)
     gemm_ffn_kernel(const GemmArgs a, const __grid_constant__ Tab tab,
                     const __grid_constant__ CUtensorMap act_map) {
-  using C = GmCfg<MODE>;
+  using C = GmCfg<QT, MODE>;
   constexpr int RB = rec_bytes(QT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -225,7 +243,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     for (int e0 = 0; e0 < a.E; e0 += 32) {
       const int e = e0 + lane;
       int v = 0;
-      if (e < a.E) v = ((a.offsets[e + 1] - a.offsets[e] + GM_TOK - 1) / GM_TOK) * a.ft_per_expert;
+      if (e < a.E) {
+        int r0, n;
+        expert_rows(a.offsets, e, a.P, a.status, r0, n);
+        v = ((n + GM_TOK - 1) / GM_TOK) * a.ft_per_expert;
+      }
       int x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -320,7 +342,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int rr = (ct >> 3) + (GM_CONV_THREADS / 8) * r;
         rowp[r] = nullptr;
         if (rr < it.n) {
-          const long long ar = a.sorted_pair ? a.sorted_pair[it.r0 + rr] / a.k : (it.r0 + rr);
+          const long long ar = row_token(a.sorted_pair, it.r0 + rr, a.k, a.T, a.status);
           rowp[r] = a.act + ar * a.act_ld + ch * 8;
         }
       }
@@ -363,14 +385,14 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
           const uint32_t tile = base_addr + slot * C::STAGE + (ri >> 3) * GM_A_TILE;
           if (MODE == 0) {
-            if (jsel) convert_record_swizzled<QT, 2, 2>(rec, tile, ri & 7, g, m);
-            else convert_record_swizzled<QT, 2, 0>(rec, tile, ri & 7, g, m);
+            if (jsel) convert_record_operand<QT, 2, 2>(rec, tile, ri & 7, g, m);
+            else convert_record_operand<QT, 2, 0>(rec, tile, ri & 7, g, m);
           } else {
             switch (jsel) {
-              case 0: convert_record_swizzled<QT, 1, 0>(rec, tile, ri & 7, g, m); break;
-              case 1: convert_record_swizzled<QT, 1, 1>(rec, tile, ri & 7, g, m); break;
-              case 2: convert_record_swizzled<QT, 1, 2>(rec, tile, ri & 7, g, m); break;
-              default: convert_record_swizzled<QT, 1, 3>(rec, tile, ri & 7, g, m); break;
+              case 0: convert_record_operand<QT, 1, 0>(rec, tile, ri & 7, g, m); break;
+              case 1: convert_record_operand<QT, 1, 1>(rec, tile, ri & 7, g, m); break;
+              case 2: convert_record_operand<QT, 1, 2>(rec, tile, ri & 7, g, m); break;
+              default: convert_record_operand<QT, 1, 3>(rec, tile, ri & 7, g, m); break;
             }
           }
         }
@@ -442,6 +464,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      // NVFP4: the operand held E2M1 x block scale; the tensor scale multiplies the sums
+      const float ts = QT == FTMOE_NVFP4 ? __ldg(reinterpret_cast<const float*>(tab.get(it.e, a) + a.rec_total))
+                                         : 1.0f;
       if (!mbar_wait_or_abort(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
@@ -459,15 +484,17 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < GM_ECOL; ++j) {
-            const float gg = __uint_as_float(gv[j]);
-            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[j]);
+            const float gg = QT == FTMOE_NVFP4 ? __uint_as_float(gv[j]) * ts : __uint_as_float(gv[j]);
+            const float uu = QT == FTMOE_NVFP4 ? __uint_as_float(uv[j]) * ts : __uint_as_float(uv[j]);
+            v[j] = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
           }
         } else {
           uint32_t yv[GM_ECOL];
           tmem_ld16(lane_base + c0, yv);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < GM_ECOL; ++j) v[j] = __uint_as_float(yv[j]);
+          for (int j = 0; j < GM_ECOL; ++j)
+            v[j] = QT == FTMOE_NVFP4 ? __uint_as_float(yv[j]) * ts : __uint_as_float(yv[j]);
         }
 #pragma unroll
         for (int p = 0; p < GM_ECOL / 2; ++p) {
@@ -538,7 +565,7 @@ static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   auto kern = gemm_ffn_kernel<QT, MODE, Tab>;
-  constexpr size_t smem = gm_smem_bytes<MODE>();
+  constexpr size_t smem = gm_smem_bytes<QT, MODE>();
   static_assert(smem <= 232448, "shared memory per CTA");
   cudaError_t err = set_smem_limit<gemm_ffn_kernel<QT, MODE, Tab>>(smem);
   if (err != cudaSuccess) return err;
@@ -559,6 +586,8 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   a.sorted_pair = pb.sorted_pair;
   a.k = pb.k;
   a.E = pb.E;
+  a.T = pb.T;
+  a.P = pb.P;
   a.status = di->status;
   a.act = pb.x;
   a.act_ld = pb.H;
@@ -572,6 +601,7 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   a.nrows = pb.I;
   a.up_row0 = pb.I;
   a.ft_per_expert = (pb.I + GM_ROWS - 1) / GM_ROWS;
+  a.rec_total = (long long)records_bytes_per_expert(pb.qtype, 2 * pb.I, pb.H);
   GemmArgs d = a;
   d.sorted_pair = nullptr;
   d.act = pb.h_act;
@@ -586,6 +616,7 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   d.nrows = pb.H;
   d.up_row0 = 0;
   d.ft_per_expert = (pb.H + GM_ROWS - 1) / GM_ROWS;
+  d.rec_total = (long long)records_bytes_per_expert(pb.qtype, pb.H, pb.I);
   cudaError_t err = gm_launch<QT, 0>(a, tab, xmap, st);
   if (err != cudaSuccess) return err;
   return gm_launch<QT, 1>(d, tab, hmap, st);
@@ -596,12 +627,16 @@ cudaError_t launch_ffn_gemm(const FfnProblem& pb, void*, size_t, cudaStream_t st
   if (pb.table) {
     GmWithTable t;
     t.t = *pb.table;
-    return pb.qtype == FTMOE_Q4_0 ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
-                                  : gm_launch_qt<FTMOE_MXFP4>(pb, t, st);
+    return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
+           : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, st)
+           : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, st)
+                                     : gm_launch_qt<FTMOE_MXFP8>(pb, t, st);
   }
   GmNoTable t;
-  return pb.qtype == FTMOE_Q4_0 ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
-                                : gm_launch_qt<FTMOE_MXFP4>(pb, t, st);
+  return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
+         : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, st)
+         : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, st)
+                                   : gm_launch_qt<FTMOE_MXFP8>(pb, t, st);
 }
 
 }  // namespace ftmoe

@@ -20,20 +20,47 @@
 // is bit-identical, so a token's output does not depend on the batch it is in.
 #include "common.cuh"
 #include "internal.h"
+#include "operand.cuh"
 #include "pipeline.cuh"
 
 namespace ftmoe {
 
-constexpr int GW_WARPS = 8;     // warps per CTA (2 CTAs per SM)
+// Launch shape (overridable at build time for sweeps): warps per CTA, CTAs per SM,
+// slabs (64 reduction elements) per stage, stages per warp.
+#ifndef FTMOE_GW_WARPS
+#define FTMOE_GW_WARPS 8
+#endif
+#ifndef FTMOE_GW_MINB
+#define FTMOE_GW_MINB 2
+#endif
+#ifndef FTMOE_GW_SL
+#define FTMOE_GW_SL 4
+#endif
+#ifndef FTMOE_GW_NS
+#define FTMOE_GW_NS 3
+#endif
+// Q4_0 A operand: biased codes 128 + q with a shared correction MMA per block (1), or
+// exact codes q - 8 through one bf16 subtract per pair (0).
+#ifndef FTMOE_GW_BIASED
+#define FTMOE_GW_BIASED 1
+#endif
+constexpr bool GW_BIASED = FTMOE_GW_BIASED != 0;
+constexpr int GW_WARPS = FTMOE_GW_WARPS;
+constexpr int GW_MINB = FTMOE_GW_MINB;
 constexpr int GW_THREADS = GW_WARPS * 32;
-constexpr int GW_SL = 4;        // slabs (64 reduction elements) per stage
-constexpr int GW_NS = 3;        // stages per warp
+constexpr int GW_SL = FTMOE_GW_SL;
+constexpr int GW_NS = FTMOE_GW_NS;
 constexpr int GW_PS = 8;        // slabs per fixed reduction part
 constexpr int GW_KPMAX = 16;    // most warps sharing one tile pair
 
+// Slabs per stage by format: MXFP8's records are twice as large, so its stages hold half
+// as many and the per-warp rings stay the same size.
+template <int QT>
+__host__ __device__ constexpr int gw_sl() { return QT == FTMOE_MXFP8 ? (GW_SL > 1 ? GW_SL / 2 : 1) : GW_SL; }
+
 template <int QT>
 struct GwSmem {
-  static constexpr int STAGE = 2 * GW_SL * rec_bytes(QT);
+  static constexpr int STAGE = 2 * gw_sl<QT>() * rec_bytes(QT);
   uint8_t stage[GW_WARPS][GW_NS][STAGE];
   uint64_t full[GW_WARPS][GW_NS];
   int16_t act[1024];
@@ -43,7 +70,7 @@ struct GwSmem {
 struct GemvArgs {
   const int32_t* offsets;
   const int32_t* sorted_pair;  // nullptr: row r is token r (k == 1)
-  int k, E;
+  int k, E, T, P;
   const uint16_t* act;  // gate/up: x [T][H]; down: h [P][I]
   int act_ld;
   uint16_t* out;        // gate/up: h [P][I]; down: y_perm [P][H]
@@ -57,6 +84,8 @@ struct GemvArgs {
   int up_rt;             // gate/up: first row tile of the up half (I / 16)
   int units_per_expert;  // gate/up: I / 16; down: H / 32
   int kp;                // part groups (warps) per unit
+  int qtype;
+  long long rec_total;   // bytes of one expert's records of this projection (NVFP4 trailer offset)
   int* counters;         // [units] arrival counters (kp > 1), zero on entry
   float* partials;       // [units][NP][256] per-part sums (kp > 1)
   int* status;
@@ -75,13 +104,15 @@ struct WithTable {
 };
 
 // Ordered list of experts with at least one row, built by every CTA from offsets.
-__device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, int16_t* s_act,
-                                                 int* s_wsum) {
+__device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, int P, int* status,
+                                                 int16_t* s_act, int* s_wsum) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int nact = 0;
   for (int e0 = 0; e0 < E; e0 += GW_THREADS) {
     const int e = e0 + threadIdx.x;
-    const bool f = e < E && offsets[e + 1] > offsets[e];
+    int r0 = 0, n = 0;
+    if (e < E) expert_rows(offsets, e, P, status, r0, n);
+    const bool f = n > 0;
     const unsigned b = __ballot_sync(0xffffffffu, f);
     if (lane == 0) s_wsum[wid] = __popc(b);
     __syncthreads();
@@ -98,22 +129,22 @@ __device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, 
   return nact;
 }
 
+// Scales of rows (g, g+8) for the blocks of a record: [b][h] as fp32 (two 32-element
+// blocks for Q4_0 / MXFP4; four 16-element blocks for NVFP4).
 template <int QT>
-__device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&a)[4]) {
-  if (QT == FTMOE_Q4_0) q4_word_to_bf16x2(w, a); else e2m1_word_to_bf16x2(w, a);
-}
-
-// Scales of rows (g, g+8) for both blocks of a record: [b][h] as fp32.
-template <int QT>
-__device__ __forceinline__ void load_scales(const uint8_t* rec, int g, float (&sc)[2][2]) {
-  if (QT == FTMOE_Q4_0) {
+__device__ __forceinline__ void load_scales(const uint8_t* rec, int g, float (&sc)[4][2]) {
+  if (QT == FTMOE_NVFP4) {
+    const uint2 s = *reinterpret_cast<const uint2*>(rec + REC_CODE_BYTES + g * 8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i >> 1][i & 1] = e4m3_to_f32(((i < 4 ? s.x : s.y) >> (8 * (i & 3))) & 0xFFu);
+  } else if (QT == FTMOE_Q4_0) {
     const uint2 s = *reinterpret_cast<const uint2*>(rec + REC_CODE_BYTES + g * 8);
     sc[0][0] = half_bits_to_f32(s.x & 0xFFFFu);
     sc[0][1] = half_bits_to_f32(s.x >> 16);
     sc[1][0] = half_bits_to_f32(s.y & 0xFFFFu);
     sc[1][1] = half_bits_to_f32(s.y >> 16);
-  } else {
-    const uint32_t s = *reinterpret_cast<const uint32_t*>(rec + REC_CODE_BYTES + g * 4);
+  } else {  // MXFP4, MXFP8: E8M0 [g][b][h] after the code bytes
+    const uint32_t s = *reinterpret_cast<const uint32_t*>(rec + rec_code_bytes(QT) + g * 4);
     sc[0][0] = e8m0_to_f32(s & 0xFFu);
     sc[0][1] = e8m0_to_f32((s >> 8) & 0xFFu);
     sc[1][0] = e8m0_to_f32((s >> 16) & 0xFFu);
@@ -131,13 +162,14 @@ struct Cursor {
   const uint8_t* w0;   // records of tile0 / tile1
   const uint8_t* w1;
   const uint16_t* brow;  // this lane's token row (B operand) for the round
+  float ts;              // NVFP4 tensor scale of the item's expert matrix (else 1)
 };
 
 template <int MODE>
 __device__ __forceinline__ void cursor_row(Cursor& c, const GemvArgs& a, int g) {
   const int rr = min(8 * c.r + g, c.n_e - 1);  // padded lanes re-read a valid row
   long long row;
-  if (MODE == 0) row = a.sorted_pair ? a.sorted_pair[c.r0 + rr] / a.k : (c.r0 + rr);
+  if (MODE == 0) row = row_token(a.sorted_pair, c.r0 + rr, a.k, a.T, a.status);
   else row = c.r0 + rr;
   c.brow = a.act + row * a.act_ld;
 }
@@ -151,8 +183,7 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const 
   const int ui = c.unit / a.units_per_expert;
   const int sub = c.unit - ui * a.units_per_expert;
   const int e = s_act[ui];
-  c.r0 = a.offsets[e];
-  c.n_e = a.offsets[e + 1] - c.r0;
+  expert_rows(a.offsets, e, a.P, nullptr, c.r0, c.n_e);  // (reported once, by the active list)
   c.tile0 = MODE == 0 ? sub : 2 * sub;
   c.tile1 = MODE == 0 ? a.up_rt + sub : 2 * sub + 1;
   c.s0 = (grp * a.NP / a.kp) * GW_PS;
@@ -162,14 +193,15 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const 
   const uint8_t* wexp = tab.get(e, a);
   c.w0 = wexp;
   c.w1 = wexp;
+  c.ts = a.qtype == FTMOE_NVFP4 ? __ldg(reinterpret_cast<const float*>(wexp + a.rec_total)) : 1.0f;
   cursor_row<MODE>(c, a, g);
 }
 
 // Next stage; returns true when the (item, round) just left is complete.
-template <int MODE, class Tab>
+template <int MODE, int SL, class Tab>
 __device__ __forceinline__ bool cursor_next(Cursor& c, const GemvArgs& a, const Tab& tab,
                                             const int16_t* s_act, int total, int nwarps, int g) {
-  c.sp += GW_SL;
+  c.sp += SL;
   if (c.sp < c.s1) return false;
   c.sp = c.s0;
   if (++c.r < (c.n_e + 7) / 8) {
@@ -182,10 +214,11 @@ __device__ __forceinline__ bool cursor_next(Cursor& c, const GemvArgs& a, const 
 }
 
 template <int QT, int MODE, class Tab>
-__global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs a,
+__global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const GemvArgs a,
                                                               const __grid_constant__ Tab tab) {
   using SM = GwSmem<QT>;
   constexpr int RB = rec_bytes(QT);
+  constexpr int SL = gw_sl<QT>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -197,7 +230,7 @@ __global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs 
   if (lane == 0)
     for (int i = 0; i < GW_NS; ++i) mbar_init(&sm.full[wid][i], 1);
   fence_barrier_init();
-  const int nact = build_active_list(a.offsets, a.E, sm.act, sm.wsum);  // contains __syncthreads
+  const int nact = build_active_list(a.offsets, a.E, a.P, a.status, sm.act, sm.wsum);  // __syncthreads inside
   const int total = nact * a.units_per_expert * a.kp;
   const int nwarps = gridDim.x * GW_WARPS;
   const int gw = blockIdx.x * GW_WARPS + wid;
@@ -215,15 +248,15 @@ __global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs 
     if (pc.item >= total) return;
     const int st = issued % GW_NS;
     if (lane == 0) {
-      const int ns = min(GW_SL, pc.s1 - pc.sp);
+      const int ns = min(SL, pc.s1 - pc.sp);
       const uint32_t bytes = (uint32_t)(ns * RB);
       mbar_arrive_expect_tx(&full[st], 2 * bytes);
       bulk_g2s(&stage[st][0], pc.w0 + pc.tile0 * tile_bytes + (long long)pc.sp * RB, bytes, &full[st]);
-      bulk_g2s(&stage[st][GW_SL * RB], pc.w1 + pc.tile1 * tile_bytes + (long long)pc.sp * RB, bytes,
+      bulk_g2s(&stage[st][SL * RB], pc.w1 + pc.tile1 * tile_bytes + (long long)pc.sp * RB, bytes,
                &full[st]);
     }
     ++issued;
-    cursor_next<MODE>(pc, a, tab, sm.act, total, nwarps, g);
+    cursor_next<MODE, SL>(pc, a, tab, sm.act, total, nwarps, g);
   };
   for (int i = 0; i < GW_NS; ++i) issue();
 
@@ -233,69 +266,139 @@ __global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs 
   Cursor cc;
   cc.item = gw;
   cursor_load<MODE>(cc, a, tab, sm.act, total, g);
-  auto load_b = [&](const Cursor& c, uint2 (&bv)[GW_SL][4]) {
+  // B operand (this lane's token row) of one slab: 4 k-steps x 2 registers
+  auto load_slab = [&](const Cursor& c, int sl, uint2 (&bv)[4]) {
     if (c.item >= total) return;
-    const uint2* base = reinterpret_cast<const uint2*>(c.brow + 4 * c4);
+    const int s = c.sp + sl;
+    if (s >= c.s1) return;
+    const bool half = ragged && s == a.S - 1;
+    const uint2* src = reinterpret_cast<const uint2*>(c.brow + 4 * c4) + s * 16;
 #pragma unroll
-    for (int sl = 0; sl < GW_SL; ++sl) {
-      const int s = c.sp + sl;
-      if (s >= c.s1) break;
-      const bool half = ragged && s == a.S - 1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j >= 2 && half) break;
-        const uint2* src = base + s * 16 + 4 * j;
-        bv[sl][j] = MODE == 0 ? __ldg(src) : __ldcg(src);
-      }
+    for (int j = 0; j < 4; ++j) {
+      if (j >= 2 && half) break;
+      bv[j] = __ldg(src + 4 * j);  // (h of the down projection: written before pdl_wait returned)
     }
   };
-  uint2 bnext[GW_SL][4];
-  load_b(cc, bnext);
+  // Warms L1 with the token-row lines of a stage: lane 4g + c takes slab c of token row g
+  // (one 128-byte line each), so the per-slab loads above hit L1.
+  auto prefetch_stage_rows = [&](const Cursor& c) {
+    if (c.item >= total) return;
+    for (int sl = c4; sl < SL && c.sp + sl < c.s1; sl += 4)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(c.brow + (long long)(c.sp + sl) * 64));
+  };
   uint32_t consumed = 0;
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // current part
   float tot[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // finished parts, in order
+  // Two slab buffers: while one slab computes, the next slab's rows load into the other
+  // (the next stage's first slab after a stage's last).  `flip` says which buffer holds
+  // the first slab of the coming stage.
+  uint2 bA[4], bB[4];
+  bool flip = false;
+  load_slab(cc, 0, bA);
   while (cc.item < total) {
-    uint2 bv[GW_SL][4];
-#pragma unroll
-    for (int sl = 0; sl < GW_SL; ++sl)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[sl][j] = bnext[sl][j];
     const Cursor cur = cc;
-    const bool done = cursor_next<MODE>(cc, a, tab, sm.act, total, nwarps, g);
-    load_b(cc, bnext);
+    const bool done = cursor_next<MODE, SL>(cc, a, tab, sm.act, total, nwarps, g);
+    prefetch_stage_rows(cc);
 
     const int st = consumed % GW_NS;
     if (!mbar_wait(&full[st], (consumed / GW_NS) & 1u, a.status)) return;
-    const int ns = min(GW_SL, cur.s1 - cur.sp);
+    const int ns = min(SL, cur.s1 - cur.sp);
+    auto stage_body = [&](uint2 (&b0)[4], uint2 (&b1)[4]) {
 #pragma unroll
-    for (int sl = 0; sl < GW_SL; ++sl) {
-      if (sl >= ns) break;
-      const int s = cur.sp + sl;
-      const bool half = ragged && s == a.S - 1;
+      for (int sl = 0; sl < SL; ++sl) {
+        if (sl >= ns) break;
+        uint2 (&bv)[4] = (sl & 1) ? b1 : b0;
+        uint2 (&bn)[4] = (sl & 1) ? b0 : b1;
+        if (sl + 1 < ns) load_slab(cur, sl + 1, bn);
+        else load_slab(cc, 0, bn);
+        const int s = cur.sp + sl;
+        const bool half = ragged && s == a.S - 1;
+        // Q4_0: the MMAs take the biased codes 128 + q; the block's -136 * sum(x) per token
+        // (the same for every weight row) comes from MMAs with a constant -136 A operand
+        // and seeds both tiles' block sums
+        float corr[2][4];
+        if (QT == FTMOE_Q4_0 && GW_BIASED) {
+          const uint32_t M136[4] = {0xC308C308u, 0xC308C308u, 0xC308C308u, 0xC308C308u};
 #pragma unroll
-      for (int ti = 0; ti < 2; ++ti) {
-        const uint8_t* rec = &stage[st][(ti * GW_SL + sl) * RB];
-        const uint4 q = *reinterpret_cast<const uint4*>(rec + lane * 16);
-        float sc[2][2];
-        load_scales<QT>(rec, g, sc);
-        const uint32_t wj[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          if (b == 1 && half) break;
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            uint32_t av[4];
-            decode_word<QT>(wj[2 * b + jj], av);
-            mma_16816(part, av, bv[sl][2 * b + jj].x, bv[sl][2 * b + jj].y);
+          for (int b = 0; b < 2; ++b) {
+            if (b == 1 && half) break;
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816_c(corr[b], M136, bv[2 * b].x, bv[2 * b].y, z);
+            mma_16816(corr[b], M136, bv[2 * b + 1].x, bv[2 * b + 1].y);
           }
-          acc[ti][0] = fmaf(sc[b][0], part[0], acc[ti][0]);
-          acc[ti][1] = fmaf(sc[b][0], part[1], acc[ti][1]);
-          acc[ti][2] = fmaf(sc[b][1], part[2], acc[ti][2]);
-          acc[ti][3] = fmaf(sc[b][1], part[3], acc[ti][3]);
+        }
+#pragma unroll
+        for (int ti = 0; ti < 2; ++ti) {
+          const uint8_t* rec = &stage[st][(ti * SL + sl) * RB];
+          float sc[4][2];
+          load_scales<QT>(rec, g, sc);
+          if (QT == FTMOE_MXFP8) {
+            // E4M3 bytes: word 2j row g, word 2j + 1 row g + 8 (elements 16j + 4c .. +3)
+            const uint4 q0 = *reinterpret_cast<const uint4*>(rec + lane * 32);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(rec + lane * 32 + 16);
+            const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              if (b == 1 && half) break;
+              float part[4];
+              const float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * b + jj;
+                const uint32_t av[4] = {e4m3x2_to_bf16x2(prmt(w8[2 * j], 0u, 0x4140u)),
+                                        e4m3x2_to_bf16x2(prmt(w8[2 * j + 1], 0u, 0x4140u)),
+                                        e4m3x2_to_bf16x2(prmt(w8[2 * j], 0u, 0x4342u)),
+                                        e4m3x2_to_bf16x2(prmt(w8[2 * j + 1], 0u, 0x4342u))};
+                if (jj == 0) mma_16816_c(part, av, bv[j].x, bv[j].y, z);
+                else mma_16816(part, av, bv[j].x, bv[j].y);
+              }
+              ffma2(acc[ti][0], acc[ti][1], sc[b][0], part[0], part[1]);
+              ffma2(acc[ti][2], acc[ti][3], sc[b][1], part[2], part[3]);
+            }
+            continue;
+          }
+          const uint4 q = *reinterpret_cast<const uint4*>(rec + lane * 16);
+          const uint32_t wj[4] = {q.x, q.y, q.z, q.w};
+          if (QT == FTMOE_NVFP4) {
+            // one 16-element block per k-step: scale every MMA's sums
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (j >= 2 && half) break;
+              float part[4];
+              uint32_t av[4];
+              const float z[4] = {0.f, 0.f, 0.f, 0.f};
+              e2m1_word_to_bf16x2(wj[j], av);
+              mma_16816_c(part, av, bv[j].x, bv[j].y, z);
+              ffma2(acc[ti][0], acc[ti][1], sc[j][0], part[0], part[1]);
+              ffma2(acc[ti][2], acc[ti][3], sc[j][1], part[2], part[3]);
+            }
+            continue;
+          }
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            if (b == 1 && half) break;
+            float part[4];
+            uint32_t av[4];
+            if (QT == FTMOE_Q4_0 && GW_BIASED) {
+              q4_word_to_biased_bf16x2(wj[2 * b], av);
+              mma_16816_c(part, av, bv[2 * b].x, bv[2 * b].y, corr[b]);
+              q4_word_to_biased_bf16x2(wj[2 * b + 1], av);
+              mma_16816(part, av, bv[2 * b + 1].x, bv[2 * b + 1].y);
+            } else {
+              const float z[4] = {0.f, 0.f, 0.f, 0.f};
+              if (QT == FTMOE_Q4_0) q4_word_to_bf16x2(wj[2 * b], av); else e2m1_word_to_bf16x2(wj[2 * b], av);
+              mma_16816_c(part, av, bv[2 * b].x, bv[2 * b].y, z);
+              if (QT == FTMOE_Q4_0) q4_word_to_bf16x2(wj[2 * b + 1], av); else e2m1_word_to_bf16x2(wj[2 * b + 1], av);
+              mma_16816(part, av, bv[2 * b + 1].x, bv[2 * b + 1].y);
+            }
+            ffma2(acc[ti][0], acc[ti][1], sc[b][0], part[0], part[1]);
+            ffma2(acc[ti][2], acc[ti][3], sc[b][1], part[2], part[3]);
+          }
         }
       }
-    }
+    };
+    if (flip) stage_body(bB, bA); else stage_body(bA, bB);
+    flip ^= (ns & 1) != 0;
     ++consumed;
     // the stage is free again: order this warp's reads before the next bulk write into it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -355,11 +458,13 @@ __global__ void __launch_bounds__(GW_THREADS, 2) gemv_ffn_kernel(const GemvArgs 
           if (rr >= cur.n_e) continue;
           const int rofs = g + 8 * (qq >> 1);
           uint16_t* orow = a.out + (long long)(cur.r0 + rr) * a.out_ld;
+          const float t0 = QT == FTMOE_NVFP4 ? tot[0][qq] * cur.ts : tot[0][qq];
+          const float t1 = QT == FTMOE_NVFP4 ? tot[1][qq] * cur.ts : tot[1][qq];
           if (MODE == 0) {
-            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(silu_f32(tot[0][qq]) * tot[1][qq]);
+            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(silu_f32(t0) * t1);
           } else {
-            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(tot[0][qq]);
-            orow[cur.tile1 * 16 + rofs] = f32_to_bf16_bits(tot[1][qq]);
+            orow[cur.tile0 * 16 + rofs] = f32_to_bf16_bits(t0);
+            orow[cur.tile1 * 16 + rofs] = f32_to_bf16_bits(t1);
           }
         }
       }
@@ -397,7 +502,7 @@ static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 // enough groups to give every warp of the GPU about two items.
 static int pick_kp(int T, long long units, int NP, int sm_count) {
   if (T > 8) return 1;
-  const long long want = 2LL * sm_count * 2 * GW_WARPS;
+  const long long want = 2LL * sm_count * GW_MINB * GW_WARPS;
   int kp = 1;
   while (kp < GW_KPMAX && units * kp < want && 2 * kp <= NP) kp *= 2;
   if (kp < NP && units * kp < want / 2) kp = NP < GW_KPMAX ? NP : GW_KPMAX;  // one part per warp
@@ -443,7 +548,7 @@ static cudaError_t launch_mode(const GemvArgs& a, const Tab& tab, int max_active
   if (err != cudaSuccess) return err;
   const long long items = (long long)max_active * a.units_per_expert * a.kp;
   long long grid = (items + GW_WARPS - 1) / GW_WARPS;
-  const long long cap = (long long)di->sm_count * 2;
+  const long long cap = (long long)di->sm_count * GW_MINB;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(GW_THREADS), smem, st, a, tab);
@@ -463,6 +568,8 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, boo
   a.sorted_pair = pb.sorted_pair;
   a.k = pb.k;
   a.E = pb.E;
+  a.T = pb.T;
+  a.P = pb.P;
   a.status = di->status;
   // gate/up + SwiGLU
   a.act = pb.x;
@@ -477,6 +584,8 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, boo
   a.NP = (a.S + GW_PS - 1) / GW_PS;
   a.up_rt = pb.I / 16;
   a.units_per_expert = pb.I / 16;
+  a.qtype = pb.qtype;
+  a.rec_total = (long long)records_bytes_per_expert(pb.qtype, 2 * pb.I, pb.H);
   a.kp = pick_kp(pb.T, (long long)max_active * a.units_per_expert, a.NP, di->sm_count);
   // down
   GemvArgs d = a;
@@ -492,6 +601,7 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, boo
   d.NP = (d.S + GW_PS - 1) / GW_PS;
   d.up_rt = 0;
   d.units_per_expert = pb.H / 32;
+  d.rec_total = (long long)records_bytes_per_expert(pb.qtype, pb.H, pb.I);
   d.kp = pick_kp(pb.T, (long long)max_active * d.units_per_expert, d.NP, di->sm_count);
   if (a.kp > 1 || d.kp > 1) {
     if (!ws || Lw.total == 0) return cudaErrorInvalidValue;
@@ -515,12 +625,16 @@ cudaError_t launch_ffn_gemv(const FfnProblem& pb, void* ws, bool ws_zeroed, cuda
   if (pb.table) {
     WithTable t;
     t.t = *pb.table;
-    return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
-                                  : launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st);
+    return pb.qtype == FTMOE_Q4_0    ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
+           : pb.qtype == FTMOE_MXFP4 ? launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st)
+           : pb.qtype == FTMOE_NVFP4 ? launch_qt<FTMOE_NVFP4>(pb, t, ws, ws_zeroed, st)
+                                     : launch_qt<FTMOE_MXFP8>(pb, t, ws, ws_zeroed, st);
   }
   NoTable t;
-  return pb.qtype == FTMOE_Q4_0 ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
-                                : launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st);
+  return pb.qtype == FTMOE_Q4_0    ? launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_zeroed, st)
+         : pb.qtype == FTMOE_MXFP4 ? launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_zeroed, st)
+         : pb.qtype == FTMOE_NVFP4 ? launch_qt<FTMOE_NVFP4>(pb, t, ws, ws_zeroed, st)
+                                   : launch_qt<FTMOE_MXFP8>(pb, t, ws, ws_zeroed, st);
 }
 
 }  // namespace ftmoe

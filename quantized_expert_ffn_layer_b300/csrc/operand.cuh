@@ -4,8 +4,9 @@
 // Two operand forms, each used by one tcgen05 kernel and reproduced element by element
 // by the verification kernels in operand_check.cu (ftmoe_dequant_operand):
 //   * the prefill grouped GEMM's A tile: every weight rounded once to bf16
-//     (round-to-nearest-even of the exact decoded value) in the 128-byte-swizzled
-//     K-major layout (convert_record_swizzled);
+//     (round-to-nearest-even of the exact decoded value; for NVFP4 the E2M1 code times
+//     its E4M3 block scale, exact, with the tensor scale left to the GEMM's epilogue) in
+//     the 128-byte-swizzled K-major layout (convert_record_swizzled);
 //   * the decode GEMM's A operand: the unscaled code value (q - 8 for Q4_0, the E2M1
 //     value for MXFP4), exact in bf16 (decode_plain).
 // Record layout: see common.cuh.
@@ -84,6 +85,8 @@ __device__ __forceinline__ uint4 e2m1_scaled8(uint32_t W, uint32_t s_hi) {
 // (Q4_0 fp16 d; lo = 0 when d is not finite, so that +-inf scales give +-inf weights and
 // NaN only where the code is q = 8), or (2^(e-127), 0) for an MXFP4 E8M0 byte
 // (e = 0 is the subnormal 2^-127, e = 255 NaN).
+// NVFP4: the E4M3 scale as bf16 (exact: 4 significant bits, in range), lo = 0; the
+// tensor scale is not part of the operand (the GEMM multiplies its accumulators by it).
 template <int QT>
 __device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t& lo2) {
   if (QT == FTMOE_Q4_0) {
@@ -92,6 +95,10 @@ __device__ __forceinline__ void row_scale(uint32_t bits, uint32_t& hi2, uint32_t
     const uint32_t lo = (bits & 0x7C00u) == 0x7C00u ? 0u : f32_to_bf16_bits(d - bf16_bits_to_f32(hi));
     hi2 = hi | (hi << 16);
     lo2 = lo | (lo << 16);
+  } else if (QT == FTMOE_NVFP4) {
+    const uint32_t b = f32_to_bf16_bits(e4m3_to_f32(bits));
+    hi2 = b | (b << 16);
+    lo2 = 0;
   } else {
     const uint32_t b = bits == 0 ? 0x0040u : (bits == 255 ? 0x7FC0u : (bits << 7));
     hi2 = b | (b << 16);
@@ -136,7 +143,9 @@ __device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi,
 template <int QT, int NSTEP, int J0>
 __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t tile, int rg, int g,
                                                         int m) {
-  constexpr int BLK = J0 >> 1;  // quantization block of the thread's steps
+  // scales per thread: one per 32-element block (Q4_0, MXFP4: both steps share it), one
+  // per step for NVFP4's 16-element blocks
+  constexpr int NSC = QT == FTMOE_NVFP4 ? NSTEP : 1;
   const int sw = (g >> 1) & 1;
   const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
   const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
@@ -146,39 +155,97 @@ __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t t
   const uint32_t row1 = row0 + 1024;
   const uint32_t ph = (uint32_t)(T0 & 7);
   // scale of row g + 8 m (this lane) and of the other row (partner lane)
-  uint32_t sbits;
-  {
-    const int idx = (g * 2 + BLK) * 2 + m;
+  uint32_t sh0[NSC], sl0[NSC], sh1[NSC], sl1[NSC];
+#pragma unroll
+  for (int u = 0; u < NSC; ++u) {
+    const int idx = QT == FTMOE_NVFP4 ? (g * 4 + J0 + u) * 2 + m : (g * 2 + (J0 >> 1)) * 2 + m;
     const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
     const uint32_t w = lds32(rec + REC_CODE_BYTES + (byte & ~3));
-    sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
+    const uint32_t sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
+    uint32_t mh, ml;
+    row_scale<QT>(sbits, mh, ml);
+    const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
+    const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
+    sh0[u] = m ? oh : mh;
+    sl0[u] = m ? ol : ml;
+    sh1[u] = m ? mh : oh;
+    sl1[u] = m ? ml : ol;
   }
-  uint32_t mh, ml;
-  row_scale<QT>(sbits, mh, ml);
-  const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
-  const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
-  const uint32_t sh0 = m ? oh : mh, sl0 = m ? ol : ml;
-  const uint32_t sh1 = m ? mh : oh, sl1 = m ? ml : ol;
   const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
   const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
   for (int s = 0; s < NSTEP; ++s) {
     const int j = J0 + s;
+    const int u = NSC > 1 ? s : 0;
     const uint32_t A = wa[j], Bw = wb[j];
     const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
     if (QT == FTMOE_Q4_0) {
       uint32_t t0[4], t1[4];
       q4_pairs(A & 0x0F0F0F0Fu, Bw & 0x0F0F0F0Fu, t0);                // row g
       q4_pairs((A >> 4) & 0x0F0F0F0Fu, (Bw >> 4) & 0x0F0F0F0Fu, t1);  // row g + 8
-      sts128(row0 + off, q4_scale(t0, sh0, sl0));
-      sts128(row1 + off, q4_scale(t1, sh1, sl1));
+      sts128(row0 + off, q4_scale(t0, sh0[u], sl0[u]));
+      sts128(row1 + off, q4_scale(t1, sh1[u], sl1[u]));
     } else {
       const uint32_t wg = (A & 0x0F0F0F0Fu) | ((Bw & 0x0F0F0F0Fu) << 4);
       const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (Bw & 0xF0F0F0F0u);
-      sts128(row0 + off, e2m1_scaled8(wg, sh0));
-      sts128(row1 + off, e2m1_scaled8(wg8, sh1));
+      sts128(row0 + off, e2m1_scaled8(wg, sh0[u]));
+      sts128(row1 + off, e2m1_scaled8(wg8, sh1[u]));
     }
   }
+}
+
+// MXFP8: the same thread roles on 1056-byte records.  Thread (g, m) writes elements
+// 8m..8m+7 of steps J0..J0+NSTEP-1 of rows g and g + 8: record lane 4g + 2m holds
+// elements 8m..8m+3 (row g in word 2j, row g + 8 in word 2j + 1) and lane 4g + 2m + 1
+// elements 8m+4..8m+7.  Each E4M3 pair becomes exact bf16 and is scaled by 2^(e - 127)
+// (one more bf16 multiply: exact unless the product leaves the bf16 range).
+template <int NSTEP, int J0>
+__device__ __forceinline__ void convert_record_swizzled_fp8(uint32_t rec, uint32_t tile, int rg, int g,
+                                                            int m) {
+  const uint32_t la = rec + (4 * g + 2 * m) * 32;
+  const int T0 = rg * 16 + gm_sigma(g);
+  const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
+  const uint32_t row1 = row0 + 1024;
+  const uint32_t ph = (uint32_t)(T0 & 7);
+  const uint32_t sw = lds32(rec + 1024 + (g * 2 + (J0 >> 1)) * 2 - ((g * 2 + (J0 >> 1)) * 2 & 3));
+  const int sb = ((g * 2 + (J0 >> 1)) * 2) & 3;
+  uint32_t s0h, s0l, s1h, s1l;
+  row_scale<FTMOE_MXFP4>((sw >> (8 * sb)) & 0xFFu, s0h, s0l);        // row g
+  row_scale<FTMOE_MXFP4>((sw >> (8 * (sb + 1))) & 0xFFu, s1h, s1l);  // row g + 8
+#pragma unroll
+  for (int s = 0; s < NSTEP; ++s) {
+    const int j = J0 + s;
+    const uint2 A = lds64(la + 8 * j);        // (row g, row g + 8) elements 8m..8m+3
+    const uint2 B = lds64(la + 32 + 8 * j);   // elements 8m+4..8m+7
+    const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
+    uint32_t r0[4], r1[4];
+    r0[0] = e4m3x2_to_bf16x2(prmt(A.x, 0u, 0x4140u));
+    r0[1] = e4m3x2_to_bf16x2(prmt(A.x, 0u, 0x4342u));
+    r0[2] = e4m3x2_to_bf16x2(prmt(B.x, 0u, 0x4140u));
+    r0[3] = e4m3x2_to_bf16x2(prmt(B.x, 0u, 0x4342u));
+    r1[0] = e4m3x2_to_bf16x2(prmt(A.y, 0u, 0x4140u));
+    r1[1] = e4m3x2_to_bf16x2(prmt(A.y, 0u, 0x4342u));
+    r1[2] = e4m3x2_to_bf16x2(prmt(B.y, 0u, 0x4140u));
+    r1[3] = e4m3x2_to_bf16x2(prmt(B.y, 0u, 0x4342u));
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      __nv_bfloat162 v0 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&r0[p]),
+                                  *reinterpret_cast<const __nv_bfloat162*>(&s0h));
+      __nv_bfloat162 v1 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&r1[p]),
+                                  *reinterpret_cast<const __nv_bfloat162*>(&s1h));
+      r0[p] = *reinterpret_cast<const uint32_t*>(&v0);
+      r1[p] = *reinterpret_cast<const uint32_t*>(&v1);
+    }
+    sts128(row0 + off, make_uint4(r0[0], r0[1], r0[2], r0[3]));
+    sts128(row1 + off, make_uint4(r1[0], r1[1], r1[2], r1[3]));
+  }
+}
+
+// Dispatch of the prefill converter on the format.
+template <int QT, int NSTEP, int J0>
+__device__ __forceinline__ void convert_record_operand(uint32_t rec, uint32_t tile, int rg, int g, int m) {
+  if (QT == FTMOE_MXFP8) convert_record_swizzled_fp8<NSTEP, J0>(rec, tile, rg, g, m);
+  else convert_record_swizzled<QT, NSTEP, J0>(rec, tile, rg, g, m);
 }
 
 // ---------------------------------------------------------------- decode GEMM A operand

@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(256) operand_prefill_kernel(const uint8_t* __r
     const int g16 = rt * 8 + rg;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (g16 < RG)
-      v = reinterpret_cast<const uint4*>(tiles + (((size_t)e * RG + g16) * S + s) * RB)[off];
+      v = reinterpret_cast<const uint4*>(tiles + (size_t)e * tiles_bytes_per_expert(QT, N, K) +
+                                         ((size_t)g16 * S + s) * RB)[off];
     reinterpret_cast<uint4*>(raw)[i] = v;
   }
   __syncthreads();
@@ -45,8 +46,8 @@ __global__ void __launch_bounds__(256) operand_prefill_kernel(const uint8_t* __r
   const int g = (lane & 15) >> 1, m = lane & 1;
   const uint32_t rec = smem_u32(raw) + ri * RB;
   const uint32_t tbase = smem_u32(tile);
-  if (warp & 1) convert_record_swizzled<QT, 2, 2>(rec, tbase, ri, g, m);
-  else convert_record_swizzled<QT, 2, 0>(rec, tbase, ri, g, m);
+  if (warp & 1) convert_record_operand<QT, 2, 2>(rec, tbase, ri, g, m);
+  else convert_record_operand<QT, 2, 0>(rec, tbase, ri, g, m);
   __syncthreads();
   // thread t: tile row t / 2, chunks 4 (t % 2) .. +3 (8 bf16 each)
   const int Tr = tid >> 1, h = tid & 1;
@@ -82,7 +83,27 @@ __global__ void operand_codes_kernel(const uint8_t* __restrict__ tiles, uint16_t
   const int rg = (int)(er % RG);
   const int e = (int)(er / RG);
   const int g = lane >> 2, c = lane & 3;
-  const uint4 q = *reinterpret_cast<const uint4*>(tiles + rec * RB + lane * 16);
+  const uint8_t* rp = tiles + (size_t)e * tiles_bytes_per_expert(QT, N, K) +
+                      (size_t)(rec - (long long)e * RG * S) * RB;
+  if (QT == FTMOE_MXFP8) {
+    // the grouped GEMV's A operand: each E4M3 element as exact bf16, unscaled
+    const uint4 q0 = *reinterpret_cast<const uint4*>(rp + lane * 32);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(rp + lane * 32 + 16);
+    const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = rg * 16 + g + 8 * h;
+        const int k = s * 64 + 16 * j + 4 * c;
+        if (k >= K) continue;
+        uint32_t* o = reinterpret_cast<uint32_t*>(out + ((size_t)e * N + row) * K + k);
+        o[0] = e4m3x2_to_bf16x2(prmt(w8[2 * j + h], 0u, 0x4140u));
+        o[1] = e4m3x2_to_bf16x2(prmt(w8[2 * j + h], 0u, 0x4342u));
+      }
+    return;
+  }
+  const uint4 q = *reinterpret_cast<const uint4*>(rp + lane * 16);
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -107,15 +128,23 @@ cudaError_t launch_operand(int qtype, int which, const void* tiles, int E, int N
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     if (qtype == FTMOE_Q4_0)
       operand_prefill_kernel<FTMOE_Q4_0><<<(unsigned)blocks, 256, 0, st>>>(t, out, E, N, K);
-    else
+    else if (qtype == FTMOE_MXFP4)
       operand_prefill_kernel<FTMOE_MXFP4><<<(unsigned)blocks, 256, 0, st>>>(t, out, E, N, K);
+    else if (qtype == FTMOE_NVFP4)
+      operand_prefill_kernel<FTMOE_NVFP4><<<(unsigned)blocks, 256, 0, st>>>(t, out, E, N, K);
+    else
+      operand_prefill_kernel<FTMOE_MXFP8><<<(unsigned)blocks, 256, 0, st>>>(t, out, E, N, K);
   } else {
     const long long threads = (long long)E * (N / 16) * slabs_of(K) * 32;
     const unsigned grid = (unsigned)((threads + 255) / 256);
     if (qtype == FTMOE_Q4_0)
       operand_codes_kernel<FTMOE_Q4_0><<<grid, 256, 0, st>>>(t, out, E, N, K);
-    else
+    else if (qtype == FTMOE_MXFP4)
       operand_codes_kernel<FTMOE_MXFP4><<<grid, 256, 0, st>>>(t, out, E, N, K);
+    else if (qtype == FTMOE_NVFP4)  // NVFP4 codes are E2M1, decoded like MXFP4's
+      operand_codes_kernel<FTMOE_NVFP4><<<grid, 256, 0, st>>>(t, out, E, N, K);
+    else
+      operand_codes_kernel<FTMOE_MXFP8><<<grid, 256, 0, st>>>(t, out, E, N, K);
   }
   return cudaGetLastError();
 }

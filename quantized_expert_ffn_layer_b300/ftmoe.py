@@ -13,7 +13,9 @@ import ctypes as C
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libftmoe.so")
+# FTMOE_LIBRARY=checks selects the bounds-checking build (libftmoe_checks.so)
+LIB_PATH = os.path.join(_HERE, "libftmoe_checks.so" if os.environ.get("FTMOE_LIBRARY") == "checks"
+                        else "libftmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -25,8 +27,8 @@ lib = C.CDLL(LIB_PATH)
 FTMOE_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "NO_SLOT",
                 5: "TIMEOUT", 6: "DEVICE_CHECK", 7: "WORKSPACE"}
-Q4_0, MXFP4 = 1, 2
-QTYPES = {"q4_0": Q4_0, "mxfp4": MXFP4}
+Q4_0, MXFP4, NVFP4, MXFP8 = 1, 2, 3, 4
+QTYPES = {"q4_0": Q4_0, "mxfp4": MXFP4, "nvfp4": NVFP4, "mxfp8": MXFP8}
 PATH_AUTO, PATH_GEMV, PATH_GEMM, PATH_GEMM_DECODE = 0, 1, 2, 3
 OPERAND_PREFILL, OPERAND_CODES = 0, 1
 LRU_PER_LAYER, LRU_GLOBAL = 0, 1

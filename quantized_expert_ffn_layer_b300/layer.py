@@ -7,9 +7,14 @@ import torch
 from . import ftmoe as F
 
 
-def upload_tiles(qtype: str, canon: np.ndarray, E: int, N: int, K: int, device, stream=None):
-    """Canonical block bytes (host numpy uint8 [E, N, K/32, blk]) -> device tiles via ftmoe_repack."""
-    src = torch.from_numpy(np.ascontiguousarray(canon).reshape(-1)).to(device)
+def upload_tiles(qtype: str, canon: np.ndarray, E: int, N: int, K: int, device, stream=None, ts=None):
+    """Canonical block bytes (host numpy uint8 [E, N, K/bs, blk]) -> device tiles via
+    ftmoe_repack; NVFP4 also takes the E fp32 tensor scales (appended to the canonical
+    buffer, as ftmoe_repack reads them)."""
+    raw = np.ascontiguousarray(canon).reshape(-1)
+    if ts is not None:
+        raw = np.concatenate([raw, np.ascontiguousarray(ts, dtype="<f4").view(np.uint8)])
+    src = torch.from_numpy(raw).to(device)
     tiles = torch.empty(F.ftmoe_tiled_bytes(qtype, E, N, K), dtype=torch.uint8, device=device)
     F.ftmoe_repack(qtype, src, tiles, E, N, K, stream)
     torch.cuda.current_stream(device).synchronize() if stream is None else stream.synchronize()
@@ -20,16 +25,19 @@ def upload_tiles(qtype: str, canon: np.ndarray, E: int, N: int, K: int, device, 
 class MoELayer:
     """One MoE layer's weights on the device in the kernels' tiled layout."""
 
-    def __init__(self, qtype, E, H, I, w13, w2, shared_w13=None, shared_w2=None, device="cuda"):
+    def __init__(self, qtype, E, H, I, w13, w2, shared_w13=None, shared_w2=None, device="cuda",
+                 ts=None):
+        """ts: NVFP4's tensor scales {"w13": [E], "w2": [E], "shared_w13": [1], "shared_w2": [1]}."""
         self.qtype, self.E, self.H, self.I = qtype, E, H, I
         self.device = torch.device(device)
-        self.w13 = upload_tiles(qtype, w13, E, 2 * I, H, self.device)
-        self.w2 = upload_tiles(qtype, w2, E, H, I, self.device)
+        t = ts or {}
+        self.w13 = upload_tiles(qtype, w13, E, 2 * I, H, self.device, ts=t.get("w13"))
+        self.w2 = upload_tiles(qtype, w2, E, H, I, self.device, ts=t.get("w2"))
         self.shared = shared_w13 is not None
         self.sw13 = self.sw2 = None
         if self.shared:
-            self.sw13 = upload_tiles(qtype, shared_w13, 1, 2 * I, H, self.device)
-            self.sw2 = upload_tiles(qtype, shared_w2, 1, H, I, self.device)
+            self.sw13 = upload_tiles(qtype, shared_w13, 1, 2 * I, H, self.device, ts=t.get("shared_w13"))
+            self.sw2 = upload_tiles(qtype, shared_w2, 1, H, I, self.device, ts=t.get("shared_w2"))
         self.weights = F.make_weights(qtype, E, H, I, self.w13, self.w2, None, self.sw13, self.sw2)
         self._ws = None
 

@@ -23,15 +23,17 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-QTYPE_BLOCK_BYTES = {"q4_0": 18, "mxfp4": 17}
+QTYPE_BLOCK_BYTES = {"q4_0": 18, "mxfp4": 17, "nvfp4": 9, "mxfp8": 33}
+QTYPE_BLOCK_ELEMS = {"q4_0": 32, "mxfp4": 32, "nvfp4": 16, "mxfp8": 32}
 BLOCK = 32
 
 # Workloads: the shapes, value distributions and seeds of the layer configs.
 CONFIGS = {
     "tiny": dict(H=256, I=128, E=8, k=2, T=64, qtype="q4_0", zipf=0.0, no_ties=True, seed=0),
     "decode": dict(H=2048, I=768, E=128, k=8, T=64, T_sweep=(1, 4, 16, 64), qtype="q4_0",
+                   qtypes=("q4_0", "mxfp4", "nvfp4", "mxfp8"),
                    zipf=0.0, no_ties=False, seed=0),
-    "prefill": dict(H=2048, I=768, E=128, k=8, T=4096, qtype="q4_0", qtypes=("q4_0", "mxfp4"),
+    "prefill": dict(H=2048, I=768, E=128, k=8, T=4096, qtype="q4_0", qtypes=("q4_0", "mxfp4", "nvfp4", "mxfp8"),
                     zipf=1.0, no_ties=False, seed=0),
     "large": dict(H=7168, I=2048, E=256, k=8, T=2048, T_total=16384, decode_T=32, qtype="mxfp4",
                   shared=True, zipf=1.0, no_ties=False, seed=0),
@@ -241,13 +243,23 @@ def quantize_mxfp8(w: np.ndarray) -> np.ndarray:
     return out.reshape(*lead, K // BLOCK, 33)
 
 
-_ENCODERS = {"q4_0": quantize_q4_0, "mxfp4": quantize_mxfp4}
+_ENCODERS = {"q4_0": quantize_q4_0, "mxfp4": quantize_mxfp4, "nvfp4": quantize_nvfp4,
+             "mxfp8": quantize_mxfp8}
 
 
 def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
                        std: float = 0.02, distinct: int | None = None,
                        threads: int = 8) -> np.ndarray:
-    """Canonical block bytes uint8 [E, N, K/32, block] of N(0, std) weights.
+    """Canonical block bytes uint8 [E, N, K/block, block bytes] (see
+    gen_expert_weights_ts, which also returns NVFP4's per-matrix tensor scales)."""
+    return gen_expert_weights_ts(seed, tag, E, N, K, qtype, std, distinct, threads)[0]
+
+
+def gen_expert_weights_ts(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
+                          std: float = 0.02, distinct: int | None = None, threads: int = 8):
+    """Canonical block bytes uint8 [E, N, K/block, block bytes] of N(0, std) weights, and
+    for NVFP4 the fp32 tensor scale of every expert's matrix (float32 [E]; None for the
+    formats without one).
 
     Expert e draws from its own stream (seed, tag, e).  With ``distinct`` < E only that
     many expert matrices are drawn (used for the largest banks, where drawing every
@@ -257,13 +269,17 @@ def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
     keeps the distribution, and no two experts hold the same matrix."""
     enc = _ENCODERS[qtype]
     nb = QTYPE_BLOCK_BYTES[qtype]
-    out = np.empty((E, N, K // BLOCK, nb), dtype=np.uint8)
+    out = np.empty((E, N, K // QTYPE_BLOCK_ELEMS[qtype], nb), dtype=np.uint8)
+    ts = np.ones(E, dtype=np.float32) if qtype == "nvfp4" else None
     D = E if distinct is None else min(distinct, E)
 
     def one(e):
         w = _rng(seed, tag, qtype, e, N, K).standard_normal((N, K), dtype=np.float32)
         w *= np.float32(std)
-        out[e] = enc(w)
+        if qtype == "nvfp4":
+            out[e], ts[e] = enc(w)
+        else:
+            out[e] = enc(w)
 
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(one, range(D)))
@@ -271,13 +287,17 @@ def gen_expert_weights(seed: int, tag: str, E: int, N: int, K: int, qtype: str,
         draws = out[:D].copy()
         src = _rng(seed, tag, "expert_src", E, D).permutation(E) % D
 
+        draws_ts = ts[:D].copy() if ts is not None else None
+
         def place(e):
             rows = _rng(seed, tag, "expert_rows", e, N).permutation(N)
             out[e] = draws[src[e]][rows]
+            if ts is not None:
+                ts[e] = draws_ts[src[e]]
 
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(place, range(E)))
-    return out
+    return out, ts
 
 
 @dataclasses.dataclass
@@ -295,22 +315,35 @@ class LayerInputs:
     w2: np.ndarray         # uint8 [E, H, I/32, blk]
     shared_w13: np.ndarray | None = None  # uint8 [1, 2I, H/32, blk]
     shared_w2: np.ndarray | None = None   # uint8 [1, H, I/32, blk]
+    # NVFP4 only: fp32 tensor scale of each expert's matrix
+    w13_ts: np.ndarray | None = None      # float32 [E]
+    w2_ts: np.ndarray | None = None       # float32 [E]
+    shared_w13_ts: np.ndarray | None = None
+    shared_w2_ts: np.ndarray | None = None
+
+    @property
+    def ts(self):
+        """The tensor scales as the oracle's layer takes them (None for formats without)."""
+        if self.w13_ts is None:
+            return None
+        return {"w13": self.w13_ts, "w2": self.w2_ts, "shared_w13": self.shared_w13_ts,
+                "shared_w2": self.shared_w2_ts}
 
 
 def make_layer(H: int, I: int, E: int, k: int, T: int, qtype: str = "q4_0", seed: int = 0,
                zipf: float = 0.0, no_ties: bool = False, shared: bool = False,
                distinct: int | None = None, std: float = 0.02, x_tag: str = "x",
                logit_tag: str = "logits", **_unused) -> LayerInputs:
-    w13 = gen_expert_weights(seed, "w13", E, 2 * I, H, qtype, std, distinct)
-    w2 = gen_expert_weights(seed, "w2", E, H, I, qtype, std, distinct)
-    sw13 = sw2 = None
+    w13, w13_ts = gen_expert_weights_ts(seed, "w13", E, 2 * I, H, qtype, std, distinct)
+    w2, w2_ts = gen_expert_weights_ts(seed, "w2", E, H, I, qtype, std, distinct)
+    sw13 = sw2 = sw13_ts = sw2_ts = None
     if shared:
-        sw13 = gen_expert_weights(seed, "shared_w13", 1, 2 * I, H, qtype, std)
-        sw2 = gen_expert_weights(seed, "shared_w2", 1, H, I, qtype, std)
+        sw13, sw13_ts = gen_expert_weights_ts(seed, "shared_w13", 1, 2 * I, H, qtype, std)
+        sw2, sw2_ts = gen_expert_weights_ts(seed, "shared_w2", 1, H, I, qtype, std)
     return LayerInputs(H, I, E, k, T, qtype,
                        gen_x_bf16(seed, T, H, x_tag),
                        gen_logits(seed, T, E, zipf, no_ties, logit_tag),
-                       w13, w2, sw13, sw2)
+                       w13, w2, sw13, sw2, w13_ts, w2_ts, sw13_ts, sw2_ts)
 
 
 def stream_trace(seed: int, steps: int, layers: int, E: int, k: int, p_repeat: float,

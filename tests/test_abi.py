@@ -29,7 +29,9 @@ def test_sizes(F):
     assert F.ftmoe_tiled_bytes("q4_0", 128, 1536, 2048) == 128 * 96 * 32 * 576
     assert F.ftmoe_tiled_bytes("mxfp4", 1, 16, 96) == 2 * 544  # ragged K: 2 records
     assert F.ftmoe_tiled_bytes("q4_0", 1, 8, 64) == 0           # N not a multiple of 16
-    assert F.ftmoe_tiled_bytes(3, 1, 16, 64) == 0
+    assert F.ftmoe_tiled_bytes("nvfp4", 1, 16, 64) == 576 + 16  # one record + tensor-scale trailer
+    assert F.ftmoe_tiled_bytes("nvfp4", 3, 32, 96) == 3 * (2 * 2 * 576 + 16)
+    assert F.ftmoe_tiled_bytes(9, 1, 16, 64) == 0                # unknown format
     assert F.ftmoe_permute_workspace_bytes(64, 8, 128) == 0
     assert F.ftmoe_permute_workspace_bytes(4096, 8, 128) == 32 * 128 * 4
     assert F.ftmoe_layer_workspace_bytes(64, 8, 128, 2048, 768, 0) > 64 * 8 * 2048 * 2

@@ -209,3 +209,47 @@ def test_acquired_slots_are_not_overwritten_before_release(env):
     st = cache.stats()
     assert st["h2d_bytes"] == nb * (st["misses"] + st["prefetch_copies"])
     cache.close()
+
+
+def test_stream_workload_trace_matches_simulator(env):
+    """The stream workload's bookkeeping at its full size: 48 layers of 128 experts, 32
+    slots per layer, the 2048-step batch-1 trace (ids repeat with p = 0.7, else Zipf 1.0),
+    the next layer prefetched while this one is acquired and released.  Every slot, hit
+    and miss of the library equals the simulator's; the totals match, and every resident
+    slot holds its blob's bytes (small stand-in blobs: the bytes' path is what is checked)."""
+    F, torch, dev = env
+    from synth import CONFIGS
+    c = CONFIGS["stream"]
+    layers, E, k, slots, steps = c["layers"], c["E"], c["k"], c["slots"], c["steps"]
+    nb = 256
+    rng = np.random.default_rng(5)
+    bank = torch.from_numpy(rng.integers(0, 256, size=(layers, E, nb), dtype=np.uint8)).pin_memory()
+    pool = torch.zeros(layers * slots * nb, dtype=torch.uint8, device=dev)
+    cache = F.ExpertCache(layers, E, nb, bank, pool, slots, F.LRU_PER_LAYER, torch.cuda.Stream(dev))
+    sim = oracle.LRUSim(layers, E, slots, "layer")
+    compute = torch.cuda.current_stream(dev)
+    trace = stream_trace(c["seed"], steps, layers, E, k, c["p_repeat"], c["zipf"]).tolist()
+    copies = 0
+    for st in range(steps):
+        got = [cache.prefetch(0, trace[st][0])[:2]]
+        want = [sim.prefetch(0, trace[st][0])]
+        for l in range(layers):
+            if l + 1 < layers:
+                got.append(cache.prefetch(l + 1, trace[st][l + 1]))
+                want.append(sim.prefetch(l + 1, trace[st][l + 1]))
+            got.append(cache.acquire(l, trace[st][l], compute)[1:])
+            want.append(sim.acquire(l, trace[st][l]))
+            cache.release(l, compute)
+            sim.release(l)
+        for (gs, gc), w in zip(got, want):
+            assert list(zip(gs, gc)) == w, st
+            copies += sum(gc)
+    stats = cache.stats()
+    assert stats["lookups"] == steps * layers * k
+    assert stats["misses"] + stats["prefetch_copies"] == copies
+    assert stats["h2d_bytes"] == nb * copies
+    torch.cuda.synchronize()
+    pool_h = pool.view(-1, nb).cpu()
+    for (l, e), s in sim.where.items():
+        assert torch.equal(pool_h[l * slots + s], bank[l, e]), (l, e, s)
+    cache.close()

@@ -188,7 +188,7 @@ def test_combine_matches_oracle(env, T, k, H, shared):
 def _layer_gpu(env, L, path=0):
     F, torch, dev = env
     from quantized_expert_ffn_layer_b300 import MoELayer
-    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev)
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev, ts=L.ts)
     old = F.ftmoe_set_ffn_path(path)
     try:
         T = L.T

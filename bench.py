@@ -100,6 +100,7 @@ KERNEL_SOURCES = {
     "expert_ffn_gemm_decode": ["gemm_decode.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
 }
 FFN_PATHS = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_decode": 3}
+LARGE_DRAWS = 16  # independent weight draws behind the large layer's 257 experts
 
 
 def kernel_src_hash(kernel: str) -> str:
@@ -195,7 +196,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "tiny"])
+    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "tiny", "large"])
     ap.add_argument("--T", type=int, default=None, help="tokens per step (default: config's)")
     ap.add_argument("--qtype", default=None)
     ap.add_argument("--ref-tokens", type=int, default=64)
@@ -208,7 +209,9 @@ def main():
     ap.add_argument("--no-gate", action="store_true", help="skip the router-gate measurement")
     ap.add_argument("--prefill-stream-chunks", type=int, default=2,
                     help="timed prefill chunks through the streamed 48-layer bank (0: skip)")
-    ap.add_argument("--stream-steps", type=int, default=256,
+    ap.add_argument("--large-steps", type=int, default=3,
+                    help="timed steps of the large-layer leg (16384-token prefill + 32-token decode; 0: skip)")
+    ap.add_argument("--stream-steps", type=int, default=2048,
                     help="timed decode steps of the 48-layer expert-cache stream (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -227,7 +230,8 @@ def main():
     cfg["workload"] = (f"{args.config} layer H{c['H']} I{c['I']} E{c['E']} top-{c['k']} "
                        f"{c['qtype']} T{c['T']}")
     # replicas draw different activations / logits, same weight distribution
-    L = make_layer(**{**c, "seed": c.get("seed", 0) + rank})
+    L = make_layer(**{**c, "seed": c.get("seed", 0) + rank},
+                   **({"distinct": LARGE_DRAWS} if args.config == "large" else {}))
 
     if args.impl == "reference":
         run_reference(args, cfg, L, world, rank)
@@ -248,6 +252,9 @@ def main():
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     pk, pk_kind = peaks()
+    if args.config == "large":
+        run_large(args, world, rank, pg, dev, flush, stream, pk, pk_kind, cfg, L)
+        return
 
     clk = ClockSampler(local_rank)
     head = measure_layer(L, dev, args.steps, args.warmup, flush, stream, pg, clk=clk)
@@ -289,11 +296,32 @@ def main():
                            "roofline": ffn_roofline(Lp, r["U"], r["ffn_ms"], pk, pk_kind, wl)}
         F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
 
+    # ---- the other bank formats on the decode layer (T as the headline): expert-FFN HBM fraction
+    formats = {}
+    if args.config == "decode" and not args.no_sweep:
+        for qt in CONFIGS["decode"]["qtypes"]:
+            if qt == L.qtype:
+                continue
+            Lq = make_layer(**{**c, "qtype": qt, "seed": c.get("seed", 0) + rank})
+            r = measure_layer(Lq, dev, max(20, args.steps // 2), 3, flush, stream, None, e2e=False)
+            formats[qt] = {"tokens_per_s": Lq.T / (np.mean(r["step_ms"]) / 1e3),
+                           "ms": float(np.mean(r["step_ms"])),
+                           "ffn_hbm_frac": ffn_roofline(Lq, r["U"], r["ffn_ms"], pk, pk_kind, "",
+                                                        args.ffn_path)["frac"]}
+
     # ---- the router gate ahead of the layer (hidden state -> logits), decode and prefill sizes
     gate = None
     if args.config == "decode" and not args.no_gate:
         gate = {f"T{Tg}": measure_gate(dev, Tg, H, E, flush, stream, pk, pk_kind, max(10, args.steps // 4))
                 for Tg in (T, CONFIGS["prefill"]["T"])}
+
+    # ---- the large layer (7168 / 2048 / 256 experts + shared, MXFP4): chunked prefill + decode
+    large = None
+    if args.config == "decode" and args.large_steps > 0:
+        F.ftmoe_set_ffn_path(FFN_PATHS["auto"])
+        large = measure_large(dev, args.large_steps, 2, flush, stream, pk, pk_kind, rank,
+                              cpu_tokens=0 if args.no_cpu_baseline else 4)
+        F.ftmoe_set_ffn_path(FFN_PATHS[args.ffn_path])
 
     # ---- batch-1 decode through 48 layers whose experts stream from a pinned-host bank
     stream_res = pstream = None
@@ -320,8 +348,49 @@ def main():
             args, world, cfg, L, value=value, step_ms=head["step_ms"], eager_ms=head["eager_ms"],
             roofline=roofline, cpu=cpu, e2e_serial=e2e_serial, e2e_pipelined=e2e_val,
             clocks=clk.summary(),
-            extras={"decode_sweep": sweep or None, "prefill": prefill, "stream": stream_res,
-                    "prefill_stream": pstream, "gate": gate})
+            extras={"decode_sweep": scalars(sweep) or None, "decode_formats": scalars(formats) or None,
+                    "prefill": scalars(prefill) or None,
+                    "large": scalars(large) or None, "stream": scalars(stream_res) or None,
+                    "prefill_stream": scalars(pstream) or None, "gate": scalars(gate) or None,
+                    "detail": {"decode_sweep": sweep or None, "decode_formats": formats or None,
+                               "prefill": prefill, "large": large,
+                               "stream": stream_res, "prefill_stream": pstream, "gate": gate}})
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_large(args, world, rank, pg, dev, flush, stream, pk, pk_kind, cfg, L):
+    """--config large: the large layer's chunked prefill is the step (value = tokens/s of
+    the 16384-token prefill, all ranks); the decode step and the oracle ride along."""
+    import torch
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    with clk:
+        r = measure_large(dev, args.steps, args.warmup, flush, stream, pk, pk_kind, rank,
+                          cpu_tokens=0 if (args.no_cpu_baseline or world > 1) else 4, L=L)
+    max_ms = max_over_ranks(pg, r["ms_per_step"] * args.steps, dev)
+    c = CONFIGS["large"]
+    value = c["T_total"] * args.steps * world / (max_ms / 1e3)
+    if rank == 0:
+        line = {"metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) activations, Zipf-skewed logits, N(0,0.02) "
+                        "weights quantized to MXFP4)",
+                "config": {"workload": r["workload"], "H": L.H, "I": L.I, "E": L.E, "k": L.k,
+                           "T": c["T_total"], "chunk": L.T, "qtype": L.qtype, "shared_expert": True,
+                           "parallelism": f"replicas{world}", "l2": "flushed between steps (512 MB write)",
+                           "step": "8 chunks of 2048 tokens, each a whole layer pass"},
+                "roofline": {"bound": r["bound"], "kernel": "whole layer (tcgen05 grouped GEMM dominant)",
+                             "achieved": r["tflops"], "peak": float(pk["bf16_tflops"]), "unit": "TFLOP/s",
+                             "frac": r["frac"], "frac_def": "t_min / t_measured, t_min = max(F / bf16 "
+                             "peak, B / HBM peak)", "traffic": None},
+                "cpu_baseline": r.get("cpu_baseline"),
+                "gpu_launches": launches_per_step(L.T * L.k, True) * (c["T_total"] // L.T) * args.steps,
+                "clocks": clk.summary(), "large": scalars(r), "detail": {"large": r}}
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -413,7 +482,7 @@ def stream_bank(L, dev):
     from quantized_expert_ffn_layer_b300 import MoELayer
     from quantized_expert_ffn_layer_b300 import ftmoe as F
     E, H, I = L.E, L.H, L.I
-    m = MoELayer(L.qtype, E, H, I, L.w13, L.w2, device=dev)
+    m = MoELayer(L.qtype, E, H, I, L.w13, L.w2, device=dev, ts=L.ts)
     nb = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
     layers = CONFIGS["stream"]["layers"]
     # the bank is pinned host memory: keep it within half of what the host has free
@@ -521,6 +590,7 @@ def measure_stream(L, dev, steps, warmup, rank, ctx):
         dd = {f: a1[f] - a0[f] for f in a1}
         modes[mode] = {"tokens_per_s": steps / (mms / 1e3), "ms_per_token": mms / steps,
                        "hit_rate": dd["hits"] / max(1, dd["lookups"]),
+                       "copy_rate": (dd["misses"] + dd["prefetch_copies"]) / steps / (layers * k),
                        "h2d_bytes_per_token": dd["h2d_bytes"] / steps,
                        "prefetch_copies_per_token": dd["prefetch_copies"] / steps}
         cache.close()
@@ -549,6 +619,11 @@ def measure_stream(L, dev, steps, warmup, rank, ctx):
              "host_wall_ms_per_token": wall_ms / steps,
              "hit_rate": d["hits"] / max(1, d["lookups"]),
              "misses_per_token": d["misses"] / steps, "prefetch_copies_per_token": d["prefetch_copies"] / steps,
+             # every blob copied, prefetched or not, per expert use: the share of the
+             # layers' expert reads that had to cross PCIe (hit_rate counts a prefetched
+             # expert as a hit, so it alone hides these copies)
+             "copies_per_token": (d["misses"] + d["prefetch_copies"]) / steps,
+             "copy_rate": (d["misses"] + d["prefetch_copies"]) / steps / (layers * k),
              "h2d_bytes_per_token": d["h2d_bytes"] / steps, "h2d_gbs": h2d_gbs,
              "pinned_copy_gbs": pcie_gbs, "h2d_frac": h2d_gbs / pcie_gbs,
              "resident_ms_per_token": res_ms / steps,
@@ -623,6 +698,123 @@ def measure_prefill_stream(dev, chunks, ctx):
             "copy_ms_per_layer": t_copy / (chunks * layers), "overlap_efficiency": overlap}
 
 
+def measure_large(dev, steps, warmup, flush, stream, pk, pk_kind, rank, cpu_tokens=0, L=None):
+    """The large MoE layer (hidden 7168, expert intermediate 2048, 256 routed experts top-8
+    plus one always-on shared expert, MXFP4, Zipf-skewed routing): a 16384-token prefill
+    run as eight 2048-token chunks, and a 32-token decode step, each step timed with CUDA
+    events on the launching stream with L2 flushed between steps.  The 257 experts' 6 GB
+    of weights come from 16 independent draws, each expert holding a draw (picked through
+    a seeded permutation) with its rows in a seeded order of its own.
+
+    Roofline per chunk: t_min = max(F / tensor peak, B / HBM peak) with F = 2 * rows * 3HI
+    (rows = 2048 * 8 routed + 2048 shared) and B = the selected experts' weights + the
+    activation rows; decode step: HBM-bound, B / HBM peak.  frac = t_min / t_measured."""
+    import torch
+    from quantized_expert_ffn_layer_b300 import MoELayer
+    from quantized_expert_ffn_layer_b300 import ftmoe as F
+    from synth import gen_logits, gen_x_bf16
+    c = dict(CONFIGS["large"])
+    if L is None:
+        L = make_layer(**{**c, "seed": c.get("seed", 0) + rank}, distinct=LARGE_DRAWS)
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev, ts=L.ts)
+    T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
+    nchunks = c["T_total"] // T
+    xs = [torch.from_numpy((L.x if ci == 0 else gen_x_bf16(rank, T, H, f"x_chunk{ci}")).view(np.int16))
+          .to(dev).view(torch.bfloat16) for ci in range(nchunks)]
+    lgs_h = [L.logits if ci == 0 else gen_logits(rank, T, E, zipf=c["zipf"], tag=f"logits_chunk{ci}")
+             for ci in range(nchunks)]
+    lgs = [torch.from_numpy(lg).to(dev) for lg in lgs_h]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ids = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(nchunks)]
+    blob = F.ftmoe_expert_blob_bytes(L.qtype, H, I)
+
+    def prefill():
+        for ci in range(nchunks):
+            m.forward(lgs[ci], xs[ci], k, out=out, ids_out=ids[ci])
+
+    def timed(fn, n):
+        ev = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for _ in range(warmup):
+        prefill()
+    torch.cuda.synchronize()
+    ms = float(np.mean(timed(prefill, steps)))
+    Us = [unique_experts(t.cpu().numpy()) for t in ids]
+    rows = T * k + T
+    flops = 2.0 * rows * 3 * H * I * nchunks
+    bytes_ = sum((u + 1) * blob for u in Us) + nchunks * (rows * H * 2 * 2 + T * H * 2)
+    hbm, tc = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    t_min = max(flops / (tc * 1e12), bytes_ / (hbm * 1e9)) * 1e3
+    res = {"workload": f"large layer H{H} I{I} E{E}+1 shared top-{k} {L.qtype}, "
+                       f"{c['T_total']}-token prefill as {nchunks} x {T}-token chunks",
+           "tokens_per_s": c["T_total"] / (ms / 1e3), "ms_per_step": ms,
+           "tflops": flops / (ms / 1e3) / 1e12, "t_min_ms": t_min, "frac": t_min / ms,
+           "bound": "tensor" if flops / (tc * 1e12) >= bytes_ / (hbm * 1e9) else "hbm",
+           "peak_kind": f"{pk_kind} bf16_tflops (burst) / hbm_gbs (copy)",
+           "unique_experts_per_chunk": float(np.mean(Us)), "alg_flops": flops, "alg_bytes": bytes_}
+    # the 32-token decode step
+    Td = c["decode_T"]
+    xd = torch.from_numpy(gen_x_bf16(rank, Td, H, "decode_x").view(np.int16)).to(dev).view(torch.bfloat16)
+    lgd_h = gen_logits(rank, Td, E, zipf=c["zipf"], tag="decode_logits")
+    lgd = torch.from_numpy(lgd_h).to(dev)
+    outd = torch.empty((Td, H), dtype=torch.bfloat16, device=dev)
+    idd = torch.empty((Td, k), dtype=torch.int32, device=dev)
+    dstep = lambda: m.forward(lgd, xd, k, out=outd, ids_out=idd)
+    for _ in range(warmup):
+        dstep()
+    torch.cuda.synchronize()
+    graph = m.capture(dstep)
+    for _ in range(warmup):
+        graph.replay()
+    dms = float(np.mean(timed(graph.replay, max(steps, 20))))
+    Ud = unique_experts(idd.cpu().numpy())
+    dbytes = (Ud + 1) * blob + Td * k * H * 2 * 2 + Td * H * 4 + Td * E * 4
+    res["decode"] = {"workload": f"large layer decode step T{Td}", "tokens_per_s": Td / (dms / 1e3),
+                     "ms_per_step": dms, "alg_bytes": dbytes, "unique_experts": Ud,
+                     "achieved_gbs": dbytes / (dms / 1e3) / 1e9,
+                     "frac": dbytes / (dms / 1e3) / 1e9 / hbm, "bound": "hbm"}
+    if cpu_tokens and rank == 0:
+        import oracle
+        try:
+            from threadpoolctl import threadpool_info
+            threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        except ImportError:
+            threads = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        oracle.layer_rows(L.x, L.logits, k, L.qtype, L.w13, L.w2, np.arange(cpu_tokens),
+                          L.shared_w13, L.shared_w2)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": cpu_tokens / dt, "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"per-token oracle on the first {cpu_tokens} tokens of "
+                                         f"chunk 0 ({dt:.1f} s)"}
+    del m
+    torch.cuda.empty_cache()
+    return res
+
+
+def scalars(d, prefix=""):
+    """The numeric fields of a nested result as one flat object {a_b_c: number}, so that a
+    reader of the one-line record sees them without descending into sub-objects."""
+    out = {}
+    for key, v in (d or {}).items():
+        name = f"{prefix}{key}"
+        if isinstance(v, dict):
+            out.update(scalars(v, name + "_"))
+        elif isinstance(v, (int, float)) and not isinstance(v, bool):
+            out[name] = v
+    return out
+
+
 def ffn_path_used(P, E, path):
     """The kernel the library runs for P pairs over E experts under path choice `path`."""
     if path == "auto":
@@ -656,6 +848,8 @@ def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload, path="auto"):
     ach = flops / (ffn_ms / 1e3) / 1e12
     return {"bound": "tensor", "kernel": "gemm_ffn_kernel x2 (tcgen05 kind::f16; gate/up+SwiGLU, down)",
             "path": used,
+            "operand": f"bf16 decoded from the {L.qtype} bank in shared memory (kind::f16 on every "
+                       "format, so the bf16 peak is the denominator; no block-scaled FP4 / FP8 MMA)",
             "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
             "peak_kind": f"{pk_kind} bf16_tflops (burst; the FFN is timed alone)",
             "traffic": recorded_traffic("expert_ffn_gemm", workload),
@@ -668,7 +862,7 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
     import torch
     from quantized_expert_ffn_layer_b300 import MoELayer
     from quantized_expert_ffn_layer_b300 import ftmoe as F
-    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev)
+    m = MoELayer(L.qtype, L.E, L.H, L.I, L.w13, L.w2, L.shared_w13, L.shared_w2, device=dev, ts=L.ts)
     T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
     P = T * k
     x = torch.from_numpy(L.x.view(np.int16)).to(dev).view(torch.bfloat16)

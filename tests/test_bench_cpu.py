@@ -66,3 +66,16 @@ def test_reference_arm_prints_on_rank_zero_only(capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_scalars_flattens_nested_numbers_for_the_one_line_record():
+    d = {"q4_0": {"tokens_per_s": 5.0, "workload": "w", "roofline": {"frac": 0.3, "unit": "TFLOP/s"}},
+         "n": 3, "flag": True, "none": None}
+    assert bench.scalars(d) == {"q4_0_tokens_per_s": 5.0, "q4_0_roofline_frac": 0.3, "n": 3}
+    assert bench.scalars(None) == {}
+
+
+def test_every_bank_format_is_a_bench_format():
+    assert set(CONFIGS["decode"]["qtypes"]) == {"q4_0", "mxfp4", "nvfp4", "mxfp8"}
+    assert set(CONFIGS["prefill"]["qtypes"]) == {"q4_0", "mxfp4", "nvfp4", "mxfp8"}
+    assert CONFIGS["stream"]["steps"] == 2048

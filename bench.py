@@ -95,9 +95,9 @@ class ClockSampler:
 
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
-    "expert_ffn_gemv": ["gemv.cu", "common.cuh", "pipeline.cuh"],
-    "expert_ffn_gemm": ["gemm_sm103.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
-    "expert_ffn_gemm_decode": ["gemm_decode.cu", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
+    "expert_ffn_gemv": ["gemv.cu", "operand.cuh", "common.cuh", "pipeline.cuh"],
+    "expert_ffn_gemm": ["gemm_sm103.cu", "operand.cuh", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
+    "expert_ffn_gemm_decode": ["gemm_decode.cu", "operand.cuh", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
 }
 FFN_PATHS = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_decode": 3}
 LARGE_DRAWS = 16  # independent weight draws behind the large layer's 257 experts

@@ -112,9 +112,16 @@ ftmoe_status run_ffn(const ftmoe_weights* wts, int E, const uint16_t* x, int T, 
   pb.h_act = fw.h_act;
   const int path = g_ffn_path;
   // measured crossovers (decode layer shape on B300): the grouped GEMV wins below about
-  // 8 rows per expert, the decode GEMM between 8 and 32, the prefill GEMM above
-  const bool many_rows = (long long)pb.P >= 32LL * E;
-  const bool mid_rows = (long long)pb.P >= 8LL * E;
+  // 8 rows per expert, the decode GEMM between 8 and 32, the prefill GEMM above.  A
+  // tensor-core path also needs work for the whole GPU: its items (token tiles of 256 or
+  // 16 rows x 128- or 256-row weight slices) must number at least half the SMs, which a
+  // single shared expert at decode sizes (E = 1, a few dozen rows) does not reach.
+  const DeviceInfo* di = device_info();
+  const long long half_sms = di ? di->sm_count / 2 : 74;
+  const long long tiles256 = ((long long)pb.P + 255) / 256 + (E > 1 ? E - 1 : 0);
+  const long long tiles16 = ((long long)pb.P + 15) / 16;
+  const bool many_rows = (long long)pb.P >= 32LL * E && tiles256 * ((pb.I + 127) / 128) >= half_sms;
+  const bool mid_rows = (long long)pb.P >= 8LL * E && tiles16 * ((pb.I + 127) / 128) >= half_sms;
   if (path == FTMOE_PATH_GEMM || (path == FTMOE_PATH_AUTO && many_rows)) {
     cudaError_t e = launch_ffn_gemm(pb, fw.gemm_ws, fw.gemm_bytes, st);
     if (e == cudaSuccess) return FTMOE_OK;
@@ -309,11 +316,18 @@ ftmoe_status ftmoe_layer(const ftmoe_weights* wts, const float* logits, const ui
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* ids = ids_out ? ids_out : L.ids;
   float* w = w_out ? w_out : L.w;
-  cudaError_t e = launch_route(logits, T, E, k, ids, w, st);
-  if (e != cudaSuccess) return FTMOE_ERR_CUDA;
-  // the permutation kernel also clears the FFN scratch that must start at zero
-  e = launch_permute(ids, T, k, E, L.offsets, L.sorted_pair, L.inv_pos, L.perm_ws, di->status,
-                     L.ffn_ws, ffn_gemv_zero_bytes(T, k, E, H, I), st);
+  // the permutation kernel also clears the FFN scratch that must start at zero; a small
+  // batch is routed by the same one-CTA launch
+  cudaError_t e;
+  if (route_permute_fits(T, k)) {
+    e = launch_route_permute(logits, T, E, k, ids, w, L.offsets, L.sorted_pair, L.inv_pos, di->status,
+                             L.ffn_ws, ffn_gemv_zero_bytes(T, k, E, H, I), st);
+  } else {
+    e = launch_route(logits, T, E, k, ids, w, st);
+    if (e == cudaSuccess)
+      e = launch_permute(ids, T, k, E, L.offsets, L.sorted_pair, L.inv_pos, L.perm_ws, di->status,
+                         L.ffn_ws, ffn_gemv_zero_bytes(T, k, E, H, I), st);
+  }
   if (e != cudaSuccess) return FTMOE_ERR_CUDA;
   ftmoe_status s = run_ffn(wts, E, x, T, k, L.offsets, L.sorted_pair, L.y_perm, wts->w13, wts->w2,
                            wts->expert_blob != nullptr, L.ffn_ws, true, st);

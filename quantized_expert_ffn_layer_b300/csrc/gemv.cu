@@ -37,7 +37,7 @@ namespace ftmoe {
 #define FTMOE_GW_SL 4
 #endif
 #ifndef FTMOE_GW_NS
-#define FTMOE_GW_NS 3
+#define FTMOE_GW_NS 2
 #endif
 // Q4_0 A operand: biased codes 128 + q with a shared correction MMA per block (1), or
 // exact codes q - 8 through one bf16 subtract per pair (0).
@@ -50,7 +50,12 @@ constexpr int GW_MINB = FTMOE_GW_MINB;
 constexpr int GW_THREADS = GW_WARPS * 32;
 constexpr int GW_SL = FTMOE_GW_SL;
 constexpr int GW_NS = FTMOE_GW_NS;
-constexpr int GW_PS = 8;        // slabs per fixed reduction part
+// slabs per fixed reduction part (a multiple of the stage's slab count)
+#ifndef FTMOE_GW_PS
+#define FTMOE_GW_PS 8
+#endif
+constexpr int GW_PS = FTMOE_GW_PS;
+static_assert(GW_PS % FTMOE_GW_SL == 0, "stages must not cross reduction parts");
 constexpr int GW_KPMAX = 16;    // most warps sharing one tile pair
 
 // Slabs per stage by format: MXFP8's records are twice as large, so its stages hold half
@@ -64,6 +69,7 @@ struct GwSmem {
   uint8_t stage[GW_WARPS][GW_NS][STAGE];
   uint64_t full[GW_WARPS][GW_NS];
   int16_t act[1024];
+  int pref[1025];  // first item of each active expert (items = tile pairs x rounds x groups)
   int wsum[GW_WARPS];
 };
 
@@ -103,9 +109,12 @@ struct WithTable {
   }
 };
 
-// Ordered list of experts with at least one row, built by every CTA from offsets.
+// Ordered list of experts with at least one row, built by every CTA from offsets, and the
+// exclusive prefix of their work items: units_per_expert x rounds (of 8 rows) x kp groups
+// each.  Returns the number of active experts; s_pref[nact] is the item total.
 __device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, int P, int* status,
-                                                 int16_t* s_act, int* s_wsum) {
+                                                 int units_per_expert, int kp, int16_t* s_act,
+                                                 int* s_pref, int* s_wsum) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int nact = 0;
   for (int e0 = 0; e0 < E; e0 += GW_THREADS) {
@@ -126,6 +135,28 @@ __device__ __forceinline__ int build_active_list(const int32_t* offsets, int E, 
     nact += tot;
     __syncthreads();
   }
+  if (wid == 0) {
+    int carry = 0;
+    for (int i0 = 0; i0 < nact; i0 += 32) {
+      const int i = i0 + lane;
+      int v = 0;
+      if (i < nact) {
+        int r0, n;
+        expert_rows(offsets, s_act[i], P, nullptr, r0, n);
+        v = units_per_expert * ((n + 7) / 8) * kp;
+      }
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (i < nact) s_pref[i] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s_pref[nact] = carry;
+  }
+  __syncthreads();
   return nact;
 }
 
@@ -152,9 +183,12 @@ __device__ __forceinline__ void load_scales(const uint8_t* rec, int g, float (&s
   }
 }
 
-// A warp's position in its flattened sequence of stages: item -> round -> stage.
+// A warp's position in its flattened sequence of stages: item -> stage.  An item is one
+// (tile pair, round of 8 rows, group of reduction parts) of an active expert, numbered
+// expert by expert with the group innermost, then the round, so that the rounds of one
+// tile pair run side by side on neighbouring warps and share its weights through L2.
 struct Cursor {
-  int item;            // unit * kp + group
+  int item;
   int unit;            // active expert * units_per_expert + sub
   int r0, n_e, tile0, tile1;
   int s0, s1;          // slab range of the item's group of parts
@@ -176,19 +210,28 @@ __device__ __forceinline__ void cursor_row(Cursor& c, const GemvArgs& a, int g) 
 
 template <int MODE, class Tab>
 __device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const Tab& tab,
-                                            const int16_t* s_act, int total, int g) {
+                                            const int16_t* s_act, const int* s_pref, int nact,
+                                            int total, int g) {
   if (c.item >= total) return;
-  c.unit = c.item / a.kp;
-  const int grp = c.item - c.unit * a.kp;
-  const int ui = c.unit / a.units_per_expert;
-  const int sub = c.unit - ui * a.units_per_expert;
+  int lo = 0, hi = nact;  // last active expert whose first item is <= item
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pref[mid] <= c.item) lo = mid; else hi = mid;
+  }
+  const int ui = lo;
   const int e = s_act[ui];
   expert_rows(a.offsets, e, a.P, nullptr, c.r0, c.n_e);  // (reported once, by the active list)
+  const int rounds = (c.n_e + 7) / 8;
+  const int local = c.item - s_pref[ui];
+  const int grp = local % a.kp;
+  const int t = local / a.kp;
+  c.r = t % rounds;
+  const int sub = t / rounds;
+  c.unit = ui * a.units_per_expert + sub;  // (kp > 1 only with one round per expert)
   c.tile0 = MODE == 0 ? sub : 2 * sub;
   c.tile1 = MODE == 0 ? a.up_rt + sub : 2 * sub + 1;
   c.s0 = (grp * a.NP / a.kp) * GW_PS;
   c.s1 = min(((grp + 1) * a.NP / a.kp) * GW_PS, a.S);
-  c.r = 0;
   c.sp = c.s0;
   const uint8_t* wexp = tab.get(e, a);
   c.w0 = wexp;
@@ -197,19 +240,15 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const 
   cursor_row<MODE>(c, a, g);
 }
 
-// Next stage; returns true when the (item, round) just left is complete.
+// Next stage; returns true when the item just left is complete.
 template <int MODE, int SL, class Tab>
 __device__ __forceinline__ bool cursor_next(Cursor& c, const GemvArgs& a, const Tab& tab,
-                                            const int16_t* s_act, int total, int nwarps, int g) {
+                                            const int16_t* s_act, const int* s_pref, int nact,
+                                            int total, int nwarps, int g) {
   c.sp += SL;
   if (c.sp < c.s1) return false;
-  c.sp = c.s0;
-  if (++c.r < (c.n_e + 7) / 8) {
-    cursor_row<MODE>(c, a, g);
-    return true;
-  }
   c.item += nwarps;
-  cursor_load<MODE>(c, a, tab, s_act, total, g);
+  cursor_load<MODE>(c, a, tab, s_act, s_pref, nact, total, g);
   return true;
 }
 
@@ -230,8 +269,9 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   if (lane == 0)
     for (int i = 0; i < GW_NS; ++i) mbar_init(&sm.full[wid][i], 1);
   fence_barrier_init();
-  const int nact = build_active_list(a.offsets, a.E, a.P, a.status, sm.act, sm.wsum);  // __syncthreads inside
-  const int total = nact * a.units_per_expert * a.kp;
+  const int nact = build_active_list(a.offsets, a.E, a.P, a.status, a.units_per_expert, a.kp, sm.act,
+                                     sm.pref, sm.wsum);  // __syncthreads inside
+  const int total = sm.pref[nact];
   const int nwarps = gridDim.x * GW_WARPS;
   const int gw = blockIdx.x * GW_WARPS + wid;
   const bool ragged = (a.K & 63) != 0;
@@ -242,7 +282,7 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   // ---- producer side (lane 0 issues the copies, every lane keeps the cursor)
   Cursor pc;
   pc.item = gw;
-  cursor_load<MODE>(pc, a, tab, sm.act, total, g);
+  cursor_load<MODE>(pc, a, tab, sm.act, sm.pref, nact, total, g);
   uint32_t issued = 0;
   auto issue = [&]() {
     if (pc.item >= total) return;
@@ -256,7 +296,7 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
                &full[st]);
     }
     ++issued;
-    cursor_next<MODE, SL>(pc, a, tab, sm.act, total, nwarps, g);
+    cursor_next<MODE, SL>(pc, a, tab, sm.act, sm.pref, nact, total, nwarps, g);
   };
   for (int i = 0; i < GW_NS; ++i) issue();
 
@@ -265,7 +305,7 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   // ---- consumer side
   Cursor cc;
   cc.item = gw;
-  cursor_load<MODE>(cc, a, tab, sm.act, total, g);
+  cursor_load<MODE>(cc, a, tab, sm.act, sm.pref, nact, total, g);
   // B operand (this lane's token row) of one slab: 4 k-steps x 2 registers
   auto load_slab = [&](const Cursor& c, int sl, uint2 (&bv)[4]) {
     if (c.item >= total) return;
@@ -297,7 +337,7 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   load_slab(cc, 0, bA);
   while (cc.item < total) {
     const Cursor cur = cc;
-    const bool done = cursor_next<MODE, SL>(cc, a, tab, sm.act, total, nwarps, g);
+    const bool done = cursor_next<MODE, SL>(cc, a, tab, sm.act, sm.pref, nact, total, nwarps, g);
     prefetch_stage_rows(cc);
 
     const int st = consumed % GW_NS;
@@ -546,7 +586,9 @@ static cudaError_t launch_mode(const GemvArgs& a, const Tab& tab, int max_active
   const size_t smem = sizeof(GwSmem<QT>);
   cudaError_t err = set_smem_limit<gemv_ffn_kernel<QT, MODE, Tab>>(smem);
   if (err != cudaSuccess) return err;
-  const long long items = (long long)max_active * a.units_per_expert * a.kp;
+  // rounds of 8 rows over all active experts: at most P / 8 + (active experts)
+  const long long rounds = (long long)a.P / 8 + max_active;
+  const long long items = rounds * a.units_per_expert * a.kp;
   long long grid = (items + GW_WARPS - 1) / GW_WARPS;
   const long long cap = (long long)di->sm_count * GW_MINB;
   if (grid > cap) grid = cap;

@@ -46,6 +46,14 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
                            int32_t* sorted_pair, int32_t* inv_pos, void* ws, int* status,
                            void* zero_ptr, size_t zero_bytes, cudaStream_t st);
 
+// Routing and permutation of a small batch in one launch (T <= ROUTE_PERMUTE_MAX_T);
+// cudaErrorNotSupported beyond that.
+constexpr int ROUTE_PERMUTE_MAX_T = 64;
+bool route_permute_fits(int T, int k);
+cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                 int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int* status,
+                                 void* zero_ptr, size_t zero_bytes, cudaStream_t st);
+
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_pos,
                            const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
                            cudaStream_t st);

@@ -8,6 +8,7 @@
 // per-chunk counts.
 #include "common.cuh"
 #include "internal.h"
+#include "route.cuh"
 
 namespace ftmoe {
 
@@ -78,12 +79,25 @@ __device__ __forceinline__ int chunk_rank(int e, int E, int* wcnt, int* chunk_cn
 }
 
 // Whole permutation in one CTA (P <= PSMALL_MAX).  Dynamic smem: (32 + 3) * E + 32 ints.
+// With EPL > 0 the CTA first routes the T = P / k tokens from `logits` (warp w takes
+// tokens w, w + 32, ...), writing ids / w, and then permutes them: routing and
+// permutation of a small batch in one launch.
+template <int EPL>
 __global__ void __launch_bounds__(PCHUNK) permute_small_kernel(const int32_t* __restrict__ ids, int P,
                                                               int E, int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ sorted_pair,
                                                               int32_t* __restrict__ inv_pos,
-                                                              int* status, int* zero_ptr, int zero_n) {
+                                                              int* status, int* zero_ptr, int zero_n,
+                                                              const float* __restrict__ logits, int k,
+                                                              float* __restrict__ wout) {
   extern __shared__ int sm[];
+  if (EPL > 0) {
+    int32_t* ids_w = const_cast<int32_t*>(ids);
+    for (int t = threadIdx.x >> 5; t < P / k; t += PCHUNK / 32)
+      route_token<(EPL > 0 ? EPL : 1)>(logits + (size_t)t * E, E, k, ids_w + (size_t)t * k,
+                                       wout + (size_t)t * k, status);
+    __syncthreads();  // the CTA's own global writes are visible to it after the barrier
+  }
   for (int i = threadIdx.x; i < zero_n; i += PCHUNK) zero_ptr[i] = 0;
   int* wcnt = sm;                 // [32][E]
   int* cnt = wcnt + 32 * E;       // [E]
@@ -205,10 +219,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   const int zero_n = zero_ptr ? (int)(zero_bytes / 4) : 0;
   if (P <= PSMALL_MAX) {
     const size_t smem = (size_t)(35 * E + 32) * sizeof(int);
-    cudaError_t err = set_smem_limit<permute_small_kernel>(smem);
+    cudaError_t err = set_smem_limit<permute_small_kernel<0>>(smem);
     if (err != cudaSuccess) return err;
-    permute_small_kernel<<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status,
-                                                (int*)zero_ptr, zero_n);
+    permute_small_kernel<0><<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status,
+                                                   (int*)zero_ptr, zero_n, nullptr, k, nullptr);
     return cudaGetLastError();
   }
   const int nchunk = (P + PCHUNK - 1) / PCHUNK;
@@ -220,6 +234,26 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   cudaError_t err = set_smem_limit<permute_scatter_kernel>(smem);
   if (err != cudaSuccess) return err;
   permute_scatter_kernel<<<nchunk, PCHUNK, smem, st>>>(ids, P, E, hist, sorted_pair, inv_pos);
+  return cudaGetLastError();
+}
+
+bool route_permute_fits(int T, int k) { return T <= ROUTE_PERMUTE_MAX_T && (long long)T * k <= PSMALL_MAX; }
+
+cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                 int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int* status,
+                                 void* zero_ptr, size_t zero_bytes, cudaStream_t st) {
+  if (!route_permute_fits(T, k)) return cudaErrorNotSupported;
+  const int P = T * k;
+  const int zero_n = zero_ptr ? (int)(zero_bytes / 4) : 0;
+  const size_t smem = (size_t)(35 * E + 32) * sizeof(int);
+  cudaError_t err = cudaSuccess;
+  with_epl(E, [&]<int N>() {
+    err = set_smem_limit<permute_small_kernel<N>>(smem);
+    if (err == cudaSuccess)
+      permute_small_kernel<N><<<1, PCHUNK, smem, st>>>(ids, P, E, offsets, sorted_pair, inv_pos, status,
+                                                     (int*)zero_ptr, zero_n, logits, k, w);
+  });
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -40,7 +40,8 @@ bool tke_ok(int T, int k, int E) {
 }
 
 // Workspace carve-up shared by ftmoe_expert_ffn and ftmoe_layer.
-// Workspace of the FFN: [gemv scratch (zero region first)][h_act][gemm scratch].
+// Workspace of the FFN: [gemv scratch (zero region first; 0 bytes: the GEMV's split
+// reductions meet in shared memory)][h_act][gemm scratch].
 struct FfnWs {
   void* gemv_ws;
   size_t gemv_zero_bytes;

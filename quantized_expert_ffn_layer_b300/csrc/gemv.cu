@@ -18,6 +18,8 @@
 // of one tile pair are spread over several warps, which write per-part sums to
 // scratch; the last warp to arrive adds them in part order.  Either way the result
 // is bit-identical, so a token's output does not depend on the batch it is in.
+#include <cstddef>
+
 #include "common.cuh"
 #include "internal.h"
 #include "operand.cuh"
@@ -71,6 +73,11 @@ struct GwSmem {
   int16_t act[1024];
   int pref[1025];  // first item of each active expert (items = tile pairs x rounds x groups)
   int wsum[GW_WARPS];
+  // split reductions (kp > 1): per warp group (GW_WARPS / kp of them) barriers "all parts
+  // written" and "read", and each warp's per-part sums of its item (at most 2 parts),
+  // last so that launches without a split leave that space to L1
+  uint64_t gfull[GW_WARPS], gfree[GW_WARPS];
+  float red[GW_WARPS][2][256];
 };
 
 struct GemvArgs {
@@ -92,8 +99,6 @@ struct GemvArgs {
   int kp;                // part groups (warps) per unit
   int qtype;
   long long rec_total;   // bytes of one expert's records of this projection (NVFP4 trailer offset)
-  int* counters;         // [units] arrival counters (kp > 1), zero on entry
-  float* partials;       // [units][NP][256] per-part sums (kp > 1)
   int* status;
 };
 
@@ -266,8 +271,14 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   if (MODE == 0) pdl_wait();  // offsets come from the permutation kernel
   pdl_launch_dependents();
 
-  if (lane == 0)
+  if (lane == 0) {
     for (int i = 0; i < GW_NS; ++i) mbar_init(&sm.full[wid][i], 1);
+    // group barriers, one per group of kp warps (initialised by the group's first warp)
+    if (a.kp > 1 && wid % a.kp == 0) {
+      mbar_init(&sm.gfull[wid], 32 * a.kp);
+      mbar_init(&sm.gfree[wid], 32);
+    }
+  }
   fence_barrier_init();
   const int nact = build_active_list(a.offsets, a.E, a.P, a.status, a.units_per_expert, a.kp, sm.act,
                                      sm.pref, sm.wsum);  // __syncthreads inside
@@ -327,6 +338,8 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
       asm volatile("prefetch.global.L1 [%0];" ::"l"(c.brow + (long long)(c.sp + sl) * 64));
   };
   uint32_t consumed = 0;
+  const int gbase = a.kp > 1 ? wid - wid % a.kp : wid;  // first warp of this warp's group
+  uint32_t red_items = 0;                               // split reductions done so far
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // current part
   float tot[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // finished parts, in order
   // Two slab buffers: while one slab computes, the next slab's rows load into the other
@@ -454,12 +467,16 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) tot[ti][qq] += acc[ti][qq];
       } else {
-        const int part = (send - 1) / GW_PS;
-        float* pb = a.partials + ((long long)cur.unit * a.NP + part) * 256;
+        // this warp's j-th part of the item: wait until the group's previous reduction has
+        // been read (its finalising warp released the buffers), then park the sums
+        const int j = (send - 1) / GW_PS - cur.s0 / GW_PS;
+        if (j == 0 && red_items > 0 &&
+            !mbar_wait(&sm.gfree[gbase], (uint32_t)((red_items - 1) & 1), a.status))
+          return;
 #pragma unroll
         for (int ti = 0; ti < 2; ++ti)
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) __stcg(pb + (ti * 4 + qq) * 32 + lane, acc[ti][qq]);
+          for (int qq = 0; qq < 4; ++qq) sm.red[wid][j][(ti * 4 + qq) * 32 + lane] = acc[ti][qq];
       }
 #pragma unroll
       for (int ti = 0; ti < 2; ++ti)
@@ -471,24 +488,27 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
       // ---- end of (item, round)
       bool finalize = true;
       if (a.kp > 1) {
-        __threadfence();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(&a.counters[cur.unit], 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        finalize = old == a.kp - 1;
+        // the group's warps (same unit, consecutive part ranges) meet in shared memory; the
+        // group's first warp adds every part in order, as one warp does without a split
+        mbar_arrive(&sm.gfull[gbase]);
+        finalize = wid == gbase;
         if (finalize) {
-          __threadfence();
-          const float* ub = a.partials + (long long)cur.unit * a.NP * 256;
+          if (!mbar_wait(&sm.gfull[gbase], (uint32_t)(red_items & 1), a.status)) return;
 #pragma unroll
           for (int ti = 0; ti < 2; ++ti)
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              float v = 0.f;
-              for (int p2 = 0; p2 < a.NP; ++p2) v += __ldcg(ub + p2 * 256 + (ti * 4 + qq) * 32 + lane);
-              tot[ti][qq] = v;
-            }
+            for (int qq = 0; qq < 4; ++qq) tot[ti][qq] = 0.f;
+          for (int gg = 0; gg < a.kp; ++gg) {
+            const int np = (gg + 1) * a.NP / a.kp - gg * a.NP / a.kp;
+            for (int j = 0; j < np; ++j)
+#pragma unroll
+              for (int ti = 0; ti < 2; ++ti)
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) tot[ti][qq] += sm.red[gbase + gg][j][(ti * 4 + qq) * 32 + lane];
+          }
+          mbar_arrive(&sm.gfree[gbase]);
         }
+        ++red_items;
       }
       if (finalize) {
         const int tok0 = 8 * cur.r;
@@ -516,10 +536,6 @@ __global__ void __launch_bounds__(GW_THREADS, GW_MINB) gemv_ffn_kernel(const Gem
   }
 }
 
-__global__ void zero_ints_kernel(int* p, int n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
-}
-
 template <class K, class... Args>
 static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args... args) {
@@ -538,54 +554,32 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Part groups per unit: only for batches of at most 8 tokens (one round per expert),
-// enough groups to give every warp of the GPU about two items.
+// Part groups per unit: only for batches of at most 8 tokens (one round per expert).
+// kp is a power of two up to GW_WARPS (so that a unit's groups are warps of one CTA) and
+// large enough that no group holds more than 2 of the NP fixed parts; beyond that it
+// grows while the GPU has fewer than about two items per warp.  1 when no such kp exists.
 static int pick_kp(int T, long long units, int NP, int sm_count) {
-  if (T > 8) return 1;
-  const long long want = 2LL * sm_count * GW_MINB * GW_WARPS;
+  if (T > 8 || NP < 2) return 1;
   int kp = 1;
-  while (kp < GW_KPMAX && units * kp < want && 2 * kp <= NP) kp *= 2;
-  if (kp < NP && units * kp < want / 2) kp = NP < GW_KPMAX ? NP : GW_KPMAX;  // one part per warp
+  while (kp < GW_WARPS && (NP + kp - 1) / kp > 2) kp *= 2;
+  if ((NP + kp - 1) / kp > 2) return 1;
+  const long long want = 2LL * sm_count * GW_MINB * GW_WARPS;
+  while (2 * kp <= GW_WARPS && 2 * kp <= NP && units * kp < want) kp *= 2;
   return kp;
 }
 
-struct GemvLayout {
-  long long u1, u2;  // units of the gate/up and down projections (upper bound)
-  int np1, np2;
-  size_t zero_bytes, total;
-  size_t off_cnt1, off_cnt2, off_p1, off_p2;
-};
-
-static GemvLayout gemv_layout(int T, int k, int E, int H, int I) {
-  GemvLayout L{};
-  if (T > 8) return L;
-  const long long mact = (long long)T * k < E ? (long long)T * k : E;
-  L.u1 = mact * (I / 16);
-  L.u2 = mact * (H / 32);
-  L.np1 = (slabs_of(H) + GW_PS - 1) / GW_PS;
-  L.np2 = (slabs_of(I) + GW_PS - 1) / GW_PS;
-  L.off_cnt1 = 0;
-  L.off_cnt2 = al256(L.u1 * 4);
-  L.zero_bytes = L.off_cnt2 + al256(L.u2 * 4);
-  L.off_p1 = L.zero_bytes;
-  L.off_p2 = L.off_p1 + al256(L.u1 * L.np1 * 1024);
-  L.total = L.off_p2 + al256(L.u2 * L.np2 * 1024);
-  return L;
-}
-
-size_t ffn_gemv_ws_bytes(int T, int k, int E, int H, int I) { return gemv_layout(T, k, E, H, I).total; }
-size_t ffn_gemv_zero_bytes(int T, int k, int E, int H, int I) {
-  return gemv_layout(T, k, E, H, I).zero_bytes;
-}
+// The split reductions meet in shared memory: the grouped GEMV needs no scratch.
+size_t ffn_gemv_ws_bytes(int, int, int, int, int) { return 0; }
+size_t ffn_gemv_zero_bytes(int, int, int, int, int) { return 0; }
 
 template <int QT, int MODE, class Tab>
 static cudaError_t launch_mode(const GemvArgs& a, const Tab& tab, int max_active, cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   auto kern = gemv_ffn_kernel<QT, MODE, Tab>;
-  const size_t smem = sizeof(GwSmem<QT>);
-  cudaError_t err = set_smem_limit<gemv_ffn_kernel<QT, MODE, Tab>>(smem);
+  cudaError_t err = set_smem_limit<gemv_ffn_kernel<QT, MODE, Tab>>(sizeof(GwSmem<QT>));
   if (err != cudaSuccess) return err;
+  const size_t smem = a.kp > 1 ? sizeof(GwSmem<QT>) : offsetof(GwSmem<QT>, red);
   // rounds of 8 rows over all active experts: at most P / 8 + (active experts)
   const long long rounds = (long long)a.P / 8 + max_active;
   const long long items = rounds * a.units_per_expert * a.kp;
@@ -602,8 +596,6 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, boo
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
   const int max_active = pb.P < pb.E ? pb.P : pb.E;
-  const GemvLayout Lw = gemv_layout(pb.T, pb.k, pb.E, pb.H, pb.I);
-  char* w = (char*)ws;
 
   GemvArgs a{};
   a.offsets = pb.offsets;
@@ -645,19 +637,6 @@ static cudaError_t launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, boo
   d.units_per_expert = pb.H / 32;
   d.rec_total = (long long)records_bytes_per_expert(pb.qtype, pb.H, pb.I);
   d.kp = pick_kp(pb.T, (long long)max_active * d.units_per_expert, d.NP, di->sm_count);
-  if (a.kp > 1 || d.kp > 1) {
-    if (!ws || Lw.total == 0) return cudaErrorInvalidValue;
-    a.counters = (int*)(w + Lw.off_cnt1);
-    a.partials = (float*)(w + Lw.off_p1);
-    d.counters = (int*)(w + Lw.off_cnt2);
-    d.partials = (float*)(w + Lw.off_p2);
-    if (!ws_zeroed) {
-      const int n = (int)(Lw.zero_bytes / 4);
-      zero_ints_kernel<<<(n + 255) / 256, 256, 0, st>>>((int*)w, n);
-      cudaError_t e0 = cudaGetLastError();
-      if (e0 != cudaSuccess) return e0;
-    }
-  }
   cudaError_t err = launch_mode<QT, 0>(a, tab, max_active, st);
   if (err != cudaSuccess) return err;
   return launch_mode<QT, 1>(d, tab, max_active, st);

@@ -194,7 +194,6 @@ __device__ __forceinline__ void load_scales(const uint8_t* rec, int g, float (&s
 // tile pair run side by side on neighbouring warps and share its weights through L2.
 struct Cursor {
   int item;
-  int unit;            // active expert * units_per_expert + sub
   int r0, n_e, tile0, tile1;
   int s0, s1;          // slab range of the item's group of parts
   int r, sp;           // round (8 tokens), first slab of the stage
@@ -232,7 +231,6 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const GemvArgs& a, const 
   const int t = local / a.kp;
   c.r = t % rounds;
   const int sub = t / rounds;
-  c.unit = ui * a.units_per_expert + sub;  // (kp > 1 only with one round per expert)
   c.tile0 = MODE == 0 ? sub : 2 * sub;
   c.tile1 = MODE == 0 ? a.up_rt + sub : 2 * sub + 1;
   c.s0 = (grp * a.NP / a.kp) * GW_PS;
@@ -554,16 +552,25 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Part groups per unit: only for batches of at most 8 tokens (one round per expert).
-// kp is a power of two up to GW_WARPS (so that a unit's groups are warps of one CTA) and
-// large enough that no group holds more than 2 of the NP fixed parts; beyond that it
-// grows while the GPU has fewer than about two items per warp.  1 when no such kp exists.
+// Split rule (overridable at build time for sweeps): largest batch whose tile pairs are
+// split over several warps, and the work items per warp the split aims for.
+#ifndef FTMOE_GW_KPT
+#define FTMOE_GW_KPT 8
+#endif
+#ifndef FTMOE_GW_IPW
+#define FTMOE_GW_IPW 2
+#endif
+
+// Part groups per unit: only for batches of at most FTMOE_GW_KPT tokens.  kp is a power
+// of two up to GW_WARPS (so that a unit's groups are warps of one CTA) and large enough
+// that no group holds more than 2 of the NP fixed parts; beyond that it grows while the
+// GPU has fewer than about FTMOE_GW_IPW items per warp.  1 when no such kp exists.
 static int pick_kp(int T, long long units, int NP, int sm_count) {
-  if (T > 8 || NP < 2) return 1;
+  if (T > FTMOE_GW_KPT || NP < 2) return 1;
   int kp = 1;
   while (kp < GW_WARPS && (NP + kp - 1) / kp > 2) kp *= 2;
   if ((NP + kp - 1) / kp > 2) return 1;
-  const long long want = 2LL * sm_count * GW_MINB * GW_WARPS;
+  const long long want = (long long)FTMOE_GW_IPW * sm_count * GW_MINB * GW_WARPS;
   while (2 * kp <= GW_WARPS && 2 * kp <= NP && units * kp < want) kp *= 2;
   return kp;
 }

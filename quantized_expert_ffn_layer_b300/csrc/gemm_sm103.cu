@@ -33,7 +33,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -76,14 +78,14 @@ constexpr int GM_MAX_E = 1024;
 #ifndef FTMOE_GM_NR1
 #define FTMOE_GM_NR1 4
 #endif
-constexpr int GM_MAX_STAGES = 8;
+constexpr int GM_MAX_STAGES = 12;
 template <int QT, int MODE>
 struct GmCfg {
   static constexpr bool FP8 = QT == FTMOE_MXFP8;
   static constexpr int NT = MODE == 0 ? 2 : 1;           // A tiles (MMAs per k-step)
   static constexpr int NACC = MODE == 0 ? 1 : 2;         // accumulator buffers
   static constexpr int NS = MODE == 0 ? (FP8 ? 2 : FTMOE_GM_NS0) : (FP8 ? 3 : FTMOE_GM_NS1);  // operand stages
-  static constexpr int NR = MODE == 0 ? (FP8 ? 3 : FTMOE_GM_NR0) : FTMOE_GM_NR1;              // raw stages
+  static constexpr int NR = MODE == 0 ? (FP8 ? 3 : FTMOE_GM_NR0) : (FP8 ? 4 : FTMOE_GM_NR1);  // raw stages
   static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES, "ring depth");
   static constexpr int NREC = 8 * NT;                    // records per stage
   static constexpr int STAGE = NT * GM_A_TILE + GM_B_TILE;
@@ -104,6 +106,9 @@ constexpr size_t gm_smem_bytes() {
          (size_t)GmCfg<QT, MODE>::NR * GmCfg<QT, MODE>::RAW_STAGE + (size_t)GM_EPI_WARPS * GM_STG +
          sizeof(GemmTail);
 }
+static_assert(gm_smem_bytes<FTMOE_Q4_0, 0>() <= 227 * 1024 && gm_smem_bytes<FTMOE_Q4_0, 1>() <= 227 * 1024 &&
+                  gm_smem_bytes<FTMOE_MXFP8, 0>() <= 227 * 1024 && gm_smem_bytes<FTMOE_MXFP8, 1>() <= 227 * 1024,
+              "shared memory per CTA");
 
 struct GemmArgs {
   const int32_t* offsets;
@@ -121,6 +126,7 @@ struct GemmArgs {
   int nrows;             // output rows of the projection's result: I or H
   int up_row0;           // gate/up: first up row of w13 (= I)
   int ft_per_expert;     // weight-row slices per token tile
+  int f_step;            // weight rows (features) per slice
   long long rec_total;   // bytes of one expert's records of this projection (NVFP4 trailer offset)
   int* status;
 };
@@ -157,7 +163,7 @@ __device__ __forceinline__ GmItem gm_item(int i, const GemmArgs& a, const int* c
   const int ft = local / ntt, tt = local - ft * ntt;
   it.r0 = beg + tt * GM_TOK;
   it.n = min(GM_TOK, ne - tt * GM_TOK);
-  it.f0 = ft * GM_ROWS;
+  it.f0 = ft * a.f_step;
   return it;
 }
 
@@ -197,6 +203,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Token rows of gate/up: gathered one stage ahead of their conversion (1), or at the
+// start of the same stage (0: the converters then wait on the MMAs of three stages back
+// instead of two).
+#ifndef FTMOE_GM_GATHER_AHEAD
+#define FTMOE_GM_GATHER_AHEAD 1
+#endif
+
+// Waits of each role: a suspending try_wait (bit clear) or a polling one (bit set) for
+// the raw-record warp (1), converters (2), MMA thread (4), epilogue (8), token warp (16).
+#ifndef FTMOE_GM_SPIN
+#define FTMOE_GM_SPIN 0
+#endif
+template <int ROLE>
+__device__ __forceinline__ bool gm_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        int* status) {
+  if (FTMOE_GM_SPIN & ROLE) return mbar_wait_spin_or_abort(bar, parity, abort_flag, status);
+  return mbar_wait_or_abort(bar, parity, abort_flag, status);
+}
+constexpr int GM_R_RAW = 1, GM_R_CONV = 2, GM_R_MMA = 4, GM_R_EPI = 8, GM_R_TOK = 16;
 
 template <int QT, int MODE, class Tab>
 __global__ void __launch_bounds__(GM_THREADS, 1)
@@ -286,7 +312,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         if (nok) prefetch_l2(tab.get(nx.e, a) + (long long)(nrow / 16) * a.S * RB, (uint32_t)(a.S * RB));
       }
       for (int kb = 0; kb < a.S; ++kb) {
-        if (!mbar_wait_or_abort(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
+        if (!gm_wait<GM_R_RAW>(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
         if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * RB));
         __syncwarp();
         if (lane < C::NREC && rok)
@@ -305,7 +331,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       for (int i = blockIdx.x; i < nitems; i += G) {
         const GmItem it = gm_item<MODE>(i, a, tl.citem);
         for (int kb = 0; kb < a.S; ++kb) {
-          if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+          if (!gm_wait<GM_R_TOK>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&tl.b_full[slot], (uint32_t)GM_B_TILE);
             tma_load_2d(base_addr + slot * C::STAGE + C::NT * GM_A_TILE, &act_map, kb * 64, it.r0,
@@ -349,7 +375,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     };
     auto issue_rows = [&]() -> bool {  // copies of stage (bi, bkb); false when none / aborted
       if (bi >= nitems) return false;
-      if (!mbar_wait_or_abort(&tl.empty[bslot], bphase ^ 1u, abort_flag, a.status)) return false;
+      if (!gm_wait<GM_R_CONV>(&tl.empty[bslot], bphase ^ 1u, abort_flag, a.status)) return false;
       const uint32_t bt = base_addr + bslot * C::STAGE + C::NT * GM_A_TILE;
       const bool kok = bkb * 64 + ch * 8 < a.K;  // beyond K: zeros
 #pragma unroll
@@ -371,16 +397,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     };
     if (MODE == 0 && bi < nitems) {
       load_rows(bi);
-      issue_rows();
+      if (FTMOE_GM_GATHER_AHEAD) issue_rows();
     }
     for (int i = blockIdx.x; i < nitems; i += G) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       bool rok;
       gm_record_row<MODE>(it, ri, a, rok);
       for (int kb = 0; kb < a.S; ++kb) {
-        const bool ahead = MODE == 0 && issue_rows();
-        if (!mbar_wait_or_abort(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
-        if (!mbar_wait_or_abort(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+        const bool ahead = MODE == 0 && issue_rows() && FTMOE_GM_GATHER_AHEAD;
+        if (!gm_wait<GM_R_CONV>(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
+        if (!gm_wait<GM_R_CONV>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         if (rok) {
           const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
           const uint32_t tile = base_addr + slot * C::STAGE + (ri >> 3) * GM_A_TILE;
@@ -417,28 +443,38 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       int slot = 0, buf = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      // Operand descriptors of slot 0, computed once: a slot's descriptors are these plus
+      // its byte offset / 16 in the start-address field (shared-memory addresses stay
+      // below 2^18, so the sum never leaves that 14-bit field).  The issue loop below is
+      // then a straight run of MMAs; scalar work between them costs issue rate.
+      uint64_t ad0[4], ad1[4], bdk[4];
+#pragma unroll
+      for (int k16 = 0; k16 < 4; ++k16) {
+        ad0[k16] = sdesc_kmajor_sw128(base_addr + 32 * k16);
+        ad1[k16] = sdesc_kmajor_sw128(base_addr + GM_A_TILE + 32 * k16);
+        bdk[k16] = sdesc_kmajor_sw128(base_addr + C::NT * GM_A_TILE + 32 * k16);
+      }
       for (int i = blockIdx.x; i < nitems && ok; i += G) {
         const GmItem it = gm_item<MODE>(i, a, tl.citem);
         const int N = max(16, (it.n + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(GM_ROWS, N);
-        if (!mbar_wait_or_abort(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
+        if (!gm_wait<GM_R_MMA>(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
         const uint32_t d0 = tmem + buf * 256;
         for (int kb = 0; kb < a.S; ++kb) {
-          if (!mbar_wait_or_abort(&tl.a_full[slot], phase, abort_flag, a.status) ||
-              (MODE == 1 && !mbar_wait_or_abort(&tl.b_full[slot], phase, abort_flag, a.status))) {
+          if (!gm_wait<GM_R_MMA>(&tl.a_full[slot], phase, abort_flag, a.status) ||
+              (MODE == 1 && !gm_wait<GM_R_MMA>(&tl.b_full[slot], phase, abort_flag, a.status))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sa = base_addr + slot * C::STAGE;
+          const uint64_t so = (uint64_t)(slot * (C::STAGE >> 4));
+          const uint32_t acc0 = kb != 0 ? 1u : 0u;  // the item's first k-step overwrites
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t bd = sdesc_kmajor_sw128(sa + C::NT * GM_A_TILE + 32 * k16);
-            const uint32_t acc = (kb | k16) ? 1u : 0u;
-            mma_bf16(d0, sdesc_kmajor_sw128(sa + 32 * k16), bd, idesc, acc);
-            if (C::NT == 2)
-              mma_bf16(d0 + 256, sdesc_kmajor_sw128(sa + GM_A_TILE + 32 * k16), bd, idesc, acc);
+            const uint32_t acc = k16 ? 1u : acc0;
+            mma_bf16(d0, ad0[k16] + so, bdk[k16] + so, idesc, acc);
+            if (C::NT == 2) mma_bf16(d0 + 256, ad1[k16] + so, bdk[k16] + so, idesc, acc);
           }
           mma_commit(&tl.empty[slot]);
           if (++slot == C::NS) { slot = 0; phase ^= 1u; }
@@ -467,7 +503,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       // NVFP4: the operand held E2M1 x block scale; the tensor scale multiplies the sums
       const float ts = QT == FTMOE_NVFP4 ? __ldg(reinterpret_cast<const float*>(tab.get(it.e, a) + a.rec_total))
                                          : 1.0f;
-      if (!mbar_wait_or_abort(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
+      if (!gm_wait<GM_R_EPI>(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
       // Each 32 x 16 block (this warp's 32 features x 16 tokens) goes through the warp's
@@ -530,6 +566,513 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   }
 }
 
+
+// ================================================================ CTA-pair kernel
+// The same grouped FFN on pairs of CTAs (a cluster of 2 on neighbouring SMs) issuing
+// tcgen05.mma.cta_group::2: one M = 256 MMA covers 256 weight rows, 128 held and
+// decoded by each CTA, against the item's up to 256 token rows, whose first half sits in
+// the first CTA's shared memory and the second half in the second's.  Every CTA's tensor
+// memory receives its 128 rows x all token columns.  Per SM this halves the token-row
+// traffic and the operand bytes the tensor core reads for a given amount of work, which
+// is what bounds the single-CTA kernel above (its stages are limited by shared-memory
+// bandwidth, not by the tensor core).
+//   gate/up item: (expert, 128 features, <= 256 tokens); CTA r decodes gate and up rows
+//     of features f0 + 64 r .. + 63, interleaved per TMEM lane quarter q: lanes 32q + t
+//     (t < 16) hold the gate row and 32q + 16 + t the up row of the same feature, so one
+//     shuffle brings g and u together in the epilogue;
+//   down item: (expert, 256 rows of H, <= 256 tokens); CTA r decodes rows f0 + 128 r ...
+// Roles per CTA as in the single-CTA kernel; the first CTA (rank 0) issues every MMA.
+// Its "operands ready" barrier counts the converter warps of both CTAs (and, for down,
+// both token warps, after their TMA box has landed); each MMA stage's commit arrives on
+// the stage's "free" barrier in both CTAs, and the accumulator barriers likewise.
+constexpr int GP_TOKH = GM_TOK / 2;           // token rows per CTA
+constexpr int GP_B_TILE = GP_TOKH * 128;      // 16 KB of bf16 (128 rows x 64)
+constexpr int GP_STAGE = GM_A_TILE + GP_B_TILE;
+#ifndef FTMOE_GP_NS
+#define FTMOE_GP_NS 5
+#endif
+#ifndef FTMOE_GP_NR
+#define FTMOE_GP_NR 4
+#endif
+// The converter warps form two groups of 8 that take alternate stages, so that the
+// latency chain of one stage's decode overlaps the other's.
+constexpr int GP_GROUP_WARPS = GM_CONV_WARPS / 2;
+// Arrivals on the first CTA's operand barrier per stage, from each CTA: the converting
+// group and the token-row warps (gate/up: the two gathering warps; down: warp 7 once the
+// TMA box has landed).  The second CTA's arrive remotely.
+template <int MODE>
+constexpr int gp_share() { return GP_GROUP_WARPS + (MODE == 0 ? 2 : 1); }
+template <int QT>
+struct GpCfg {
+  static constexpr int NS = FTMOE_GP_NS;  // operand stages
+  static constexpr int NR = FTMOE_GP_NR;  // raw-record stages
+  static constexpr int AHEAD = 2;         // gate/up token rows gathered this many stages ahead
+  static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES && AHEAD < NS, "ring depth");
+  static constexpr int NREC = 8;          // records per stage (128 rows)
+  static constexpr int RAW_STAGE = NREC * rec_bytes(QT);
+};
+template <int QT>
+constexpr size_t gp_smem_bytes() {
+  return 1024 + (size_t)GpCfg<QT>::NS * GP_STAGE + (size_t)GpCfg<QT>::NR * GpCfg<QT>::RAW_STAGE +
+         (size_t)GM_EPI_WARPS * GM_STG + sizeof(GemmTail);
+}
+static_assert(gp_smem_bytes<FTMOE_Q4_0>() <= 227 * 1024 && gp_smem_bytes<FTMOE_MXFP8>() <= 227 * 1024,
+              "shared memory per CTA");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrival on a barrier of either CTA of the pair (default semantics: release at CTA
+// scope, the form used for cross-CTA pipeline barriers; a cluster-scope release also
+// waits for this thread's outstanding copies, which costs the converters a stage).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// A role's share of stage `slot` is ready: arrive on the first CTA's operand barrier.
+__device__ __forceinline__ void gp_arrive_ready(uint64_t* a_full, int slot, uint32_t rank) {
+  if (rank == 0) mbar_arrive(&a_full[slot]);
+  else mbar_arrive_remote(cluster_addr(&a_full[slot], 0));
+}
+// Bounded wait on a local barrier that also receives arrivals from the other CTA.
+__device__ __forceinline__ bool gp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                int* status, uint64_t limit_ns = 2000000000ull) {
+  auto try_once = [&](uint32_t hint) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once(0u)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (try_once(FTMOE_WAIT_HINT_NS)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      set_device_code(status, DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` in every CTA of `mask` when the pair's MMAs issued so far complete.
+__device__ __forceinline__ void mma2_commit(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+// First matrix row of record ri (0..7) of CTA `rank`'s half of an item, and whether it
+// lies inside the projection's result rows.
+template <int MODE>
+__device__ __forceinline__ int gp_record_row(const GmItem& it, int ri, uint32_t rank, const GemmArgs& a,
+                                             bool& ok) {
+  if (MODE == 0) {
+    const int f = it.f0 + 64 * (int)rank + 16 * (ri >> 1);  // first feature of the record
+    ok = f < a.nrows;
+    return (ri & 1) ? f + a.up_row0 : f;
+  }
+  const int row = it.f0 + 128 * (int)rank + 16 * ri;
+  ok = row < a.nrows;
+  return row;
+}
+
+template <int QT, int MODE, class Tab>
+__global__ void __launch_bounds__(GM_THREADS, 1)
+    gemm_pair_kernel(const GemmArgs a, const __grid_constant__ Tab tab,
+                     const __grid_constant__ CUtensorMap act_map) {
+  using C = GpCfg<QT>;
+  constexpr int RB = rec_bytes(QT);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_addr - raw_addr);
+  const uint32_t rawring = base_addr + C::NS * GP_STAGE;
+  const uint32_t staging = rawring + C::NR * C::RAW_STAGE;
+  GemmTail& tl = *reinterpret_cast<GemmTail*>(base + (size_t)C::NS * GP_STAGE +
+                                              (size_t)C::NR * C::RAW_STAGE + GM_EPI_WARPS * GM_STG);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &tl.abort_flag;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&tl.a_full[s], 2 * gp_share<MODE>());
+      mbar_init(&tl.b_full[s], 1);
+      mbar_init(&tl.empty[s], 1);
+    }
+    for (int s = 0; s < C::NR; ++s) {
+      mbar_init(&tl.raw_full[s], 1);
+      mbar_init(&tl.raw_empty[s], GP_GROUP_WARPS);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tl.acc_full[b], 1);
+      mbar_init(&tl.acc_empty[b], 2 * GM_EPI_WARPS);
+    }
+    mbar_init(&tl.drain, 1);
+    tl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == GM_MMA_WARP) {
+    // collective over the pair: both CTAs allocate, and both receive the same columns
+    tmem_alloc2(&tl.tmem_base, GM_TMEM_COLS);
+    tmem_relinquish2();
+  }
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+      const int e = e0 + lane;
+      int v = 0;
+      if (e < a.E) {
+        int r0, n;
+        expert_rows(a.offsets, e, a.P, a.status, r0, n);
+        v = ((n + GM_TOK - 1) / GM_TOK) * a.ft_per_expert;
+      }
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (e < a.E) tl.citem[e] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) tl.citem[a.E] = carry;
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after_sync();
+  const uint32_t tmem = tl.tmem_base;
+  const int nitems = tl.citem[a.E];
+
+  if (warp == GM_RAW_WARP) {
+    // ------------------------------------------------------------ raw weight records
+    int rslot = 0;
+    uint32_t rphase = 0;
+    for (int i = pair; i < nitems; i += npairs) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      bool rok = false;
+      const uint8_t* rec0 = nullptr;
+      if (lane < C::NREC) rec0 = tab.get(it.e, a) + (long long)(gp_record_row<MODE>(it, lane, rank, a, rok) / 16) * a.S * RB;
+      const int nrec = __popc(__ballot_sync(0xffffffffu, lane < C::NREC && rok));
+      if (i + npairs < nitems && lane < C::NREC) {
+        const GmItem nx = gm_item<MODE>(i + npairs, a, tl.citem);
+        bool nok;
+        const int nrow = gp_record_row<MODE>(nx, lane, rank, a, nok);
+        if (nok) prefetch_l2(tab.get(nx.e, a) + (long long)(nrow / 16) * a.S * RB, (uint32_t)(a.S * RB));
+      }
+      for (int kb = 0; kb < a.S; ++kb) {
+        if (!gm_wait<GM_R_RAW>(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * RB));
+        __syncwarp();
+        if (lane < C::NREC && rok)
+          bulk_g2s(base + C::NS * GP_STAGE + rslot * C::RAW_STAGE + lane * RB, rec0 + (long long)kb * RB, RB,
+                   &tl.raw_full[rslot]);
+        if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
+      }
+      if (*abort_flag) break;
+    }
+  } else if (MODE == 0 && (warp == GM_TOK_WARP || warp == GM_TOK_WARP + 1)) {
+    // ------------------------------------------------------------ token rows, gate/up
+    // this CTA's half of the item's x rows, gathered through the permutation with
+    // cp.async AHEAD stages ahead; a stage is reported to the first CTA's operand barrier
+    // once its copies have landed.  Thread gt copies 16-byte chunk (gt & 7) of B rows
+    // (gt >> 3) + 8 r.
+    const int gt = tid - GM_TOK_WARP * 32;
+    constexpr int GR = GP_TOKH * 8 / 64;  // rows per thread
+    const int ch = gt & 7;
+    const uint16_t* rowp[GR];
+    int slot = 0, done_slot = 0, inflight = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = pair; i < nitems && ok; i += npairs) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      const int half = max(16, (it.n + 15) & ~15) / 2;
+#pragma unroll
+      for (int r = 0; r < GR; ++r) {
+        const int rr = (gt >> 3) + 8 * r;
+        const int tk = (int)rank * half + rr;  // token of the item held in B row rr
+        rowp[r] = nullptr;
+        if (rr < half && tk < it.n) {
+          const long long ar = row_token(a.sorted_pair, it.r0 + tk, a.k, a.T, a.status);
+          rowp[r] = a.act + ar * a.act_ld + ch * 8;
+        }
+      }
+      for (int kb = 0; kb < a.S; ++kb) {
+        if (!gm_wait<GM_R_TOK>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bt = base_addr + slot * GP_STAGE + GM_A_TILE;
+        const bool kok = kb * 64 + ch * 8 < a.K;  // beyond K: zeros
+#pragma unroll
+        for (int r = 0; r < GR; ++r) {
+          if (rowp[r]) {
+            const int rr = (gt >> 3) + 8 * r;
+            cp_async16(bt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16),
+                       kok ? rowp[r] + kb * 64 : rowp[r], kok ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+        if (++inflight > C::AHEAD) {
+          cp_async_wait<C::AHEAD>();
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) gp_arrive_ready(tl.a_full, done_slot, rank);
+          if (++done_slot == C::NS) done_slot = 0;
+          --inflight;
+        }
+      }
+      if (*abort_flag) break;
+    }
+    cp_async_wait<0>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    for (; inflight > 0 && ok && !*abort_flag; --inflight) {
+      if (lane == 0) gp_arrive_ready(tl.a_full, done_slot, rank);
+      if (++done_slot == C::NS) done_slot = 0;
+    }
+  } else if (warp == GM_TOK_WARP || warp == GM_TOK_WARP + 1) {
+    // ------------------------------------------------------------ token rows, down projection
+    // this CTA's half of the item's h rows: one 64 x 128 TMA box per stage, issued by
+    // warp 6 as soon as the stage is free; warp 7 reports each landed box to the first
+    // CTA's operand barrier, so that several boxes stay in flight
+    if (MODE == 1) {
+      const bool issuer = warp == GM_TOK_WARP;
+      int slot = 0;
+      uint32_t phase = 0;
+      for (int i = pair; i < nitems; i += npairs) {
+        const GmItem it = gm_item<MODE>(i, a, tl.citem);
+        const int half = max(16, (it.n + 15) & ~15) / 2;
+        for (int kb = 0; kb < a.S; ++kb) {
+          if (issuer) {
+            if (!gm_wait<GM_R_TOK>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&tl.b_full[slot], (uint32_t)GP_B_TILE);
+              tma_load_2d(base_addr + slot * GP_STAGE + GM_A_TILE, &act_map, kb * 64, it.r0 + (int)rank * half,
+                          &tl.b_full[slot]);
+            }
+          } else {
+            if (!gm_wait<GM_R_TOK>(&tl.b_full[slot], phase, abort_flag, a.status)) break;
+            if (lane == 0) gp_arrive_ready(tl.a_full, slot, rank);
+          }
+          if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+        }
+        if (*abort_flag) break;
+      }
+    }
+  } else if (warp >= GM_CONV0) {
+    // ------------------------------------------------------------ converters
+    // group cw / 8 converts the stages of its parity; in a stage, warp cw % 8 converts
+    // records 2 (cw % 4) + {0, 1} (half-warps), quantization block (cw / 4) % 2
+    const int ct = tid - GM_CONV0 * 32;
+    const int cw = ct >> 5;
+    const int grp = cw / GP_GROUP_WARPS;
+    const int ri = 2 * (cw & 3) + (lane >> 4);
+    const int jsel = (cw >> 2) & 1;
+    const int g = (lane & 15) >> 1, m = lane & 1;
+    int t = 0;  // stage number in this pair's sequence
+    for (int i = pair; i < nitems; i += npairs) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      bool rok;
+      gp_record_row<MODE>(it, ri, rank, a, rok);
+      for (int kb = 0; kb < a.S; ++kb, ++t) {
+        if ((t & 1) != grp) continue;
+        const int slot = t % C::NS, rslot = t % C::NR;
+        const uint32_t phase = (uint32_t)(t / C::NS) & 1u, rphase = (uint32_t)(t / C::NR) & 1u;
+        if (!gm_wait<GM_R_CONV>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
+        if (!gm_wait<GM_R_CONV>(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
+        if (rok) {
+          const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
+          const uint32_t st_base = base_addr + slot * GP_STAGE;
+          if (jsel) convert_record_operand<QT, 2, 2>(rec, st_base, ri, g, m);
+          else convert_record_operand<QT, 2, 0>(rec, st_base, ri, g, m);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tl.raw_empty[rslot]);
+          gp_arrive_ready(tl.a_full, slot, rank);
+        }
+      }
+      if (*abort_flag) break;
+    }
+  } else if (warp == GM_MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue (first CTA)
+    if (rank == 0 && lane == 0) {
+      int slot = 0, buf = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      uint64_t adk[4], bdk[4];
+#pragma unroll
+      for (int k16 = 0; k16 < 4; ++k16) {
+        adk[k16] = sdesc_kmajor_sw128(base_addr + 32 * k16);
+        bdk[k16] = sdesc_kmajor_sw128(base_addr + GM_A_TILE + 32 * k16);
+      }
+      for (int i = pair; i < nitems && ok; i += npairs) {
+        const GmItem it = gm_item<MODE>(i, a, tl.citem);
+        const int N = max(16, (it.n + 15) & ~15);
+        const uint32_t idesc = idesc_bf16_f32(2 * GM_ROWS, N);
+        if (!gp_wait_cluster(&tl.acc_empty[buf], acc_phase ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem + buf * 256;
+        for (int kb = 0; kb < a.S; ++kb) {
+          if (!gp_wait_cluster(&tl.a_full[slot], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t so = (uint64_t)(slot * (GP_STAGE >> 4));
+          const uint32_t acc0 = kb != 0 ? 1u : 0u;
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16) mma2_bf16(d0, adk[k16] + so, bdk[k16] + so, idesc, k16 ? 1u : acc0);
+          mma2_commit(&tl.empty[slot], 3);
+          if (++slot == C::NS) { slot = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma2_commit(&tl.acc_full[buf], 3);
+        if (++buf == 2) { buf = 0; acc_phase ^= 1u; }
+      }
+      mma2_commit(&tl.drain, 1);
+      mbar_wait_or_abort(&tl.drain, 0, abort_flag, a.status, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp < GM_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue (warps 0..3)
+    const int q = warp;
+    const uint32_t stg = staging + q * GM_STG;
+    const uint32_t lead_accempty = cluster_addr(&tl.acc_empty[0], 0);
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int i = pair; i < nitems; i += npairs) {
+      const GmItem it = gm_item<MODE>(i, a, tl.citem);
+      const float ts = QT == FTMOE_NVFP4 ? __ldg(reinterpret_cast<const float*>(tab.get(it.e, a) + a.rec_total))
+                                         : 1.0f;
+      if (!gm_wait<GM_R_EPI>(&tl.acc_full[buf], acc_phase, abort_flag, a.status)) break;
+      tc_fence_after_sync();
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
+      if (MODE == 0) {
+        // lanes t and t + 16 hold the gate and up sums of feature fw + sigma^-1(t); after
+        // one exchange lane t computes tokens c0..c0+7 and lane t + 16 tokens c0+8..c0+15
+        const int fw = it.f0 + 64 * (int)rank + 16 * q;
+        const int fl = gm_sigma_inv(lane & 15);
+        const int hi = lane >> 4;
+        const bool ok = fw < a.nrows;
+        for (int c0 = 0; c0 < it.n; c0 += GM_ECOL) {
+          uint32_t v[GM_ECOL];
+          tmem_ld16(lane_base + c0, v);
+          tmem_wait_ld();
+          float h[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            // lane t sends its column 8 + j (needed by t + 16), lane t + 16 its column j
+            const uint32_t send = hi ? v[j] : v[8 + j];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float gg = __uint_as_float(hi ? recv : v[j]) * ts;
+            const float uu = __uint_as_float(hi ? v[8 + j] : recv) * ts;
+            h[j] = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stg + (8 * hi + j) * 32 + fl * 2),
+                         "h"(f32_to_bf16_bits(h[j]))
+                         : "memory");
+          __syncwarp();
+          const int row = lane >> 1;
+          const uint4 d = lds128(stg + row * 32 + (lane & 1) * 16);
+          if (ok && c0 + row < it.n)
+            *reinterpret_cast<uint4*>(a.out + (long long)(it.r0 + c0 + row) * a.out_ld + fw + 8 * (lane & 1)) = d;
+          __syncwarp();
+        }
+      } else {
+        // lanes hold rows fw + fl of H; lanes l and l ^ 2 hold adjacent rows fl and fl ^ 1
+        const int fl = (lane & 16) + gm_sigma_inv(lane & 15);
+        const int odd = fl & 1;
+        const int fw = it.f0 + 128 * (int)rank + 32 * q;
+        const bool ok = fw < a.nrows;
+        uint16_t* obase = a.out + (long long)it.r0 * a.out_ld + fw + 8 * (lane & 3);
+        for (int c0 = 0; c0 < it.n; c0 += GM_ECOL) {
+          uint32_t yv[GM_ECOL];
+          tmem_ld16(lane_base + c0, yv);
+          tmem_wait_ld();
+          float v[GM_ECOL];
+#pragma unroll
+          for (int j = 0; j < GM_ECOL; ++j) v[j] = __uint_as_float(yv[j]) * ts;
+#pragma unroll
+          for (int p = 0; p < GM_ECOL / 2; ++p) {
+            const float send = odd ? v[2 * p] : v[2 * p + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
+            const float lo = odd ? recv : v[2 * p];
+            const float hv = odd ? v[2 * p + 1] : recv;
+            const uint32_t w = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hv) << 16);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + (2 * p + odd) * 64 + (fl & ~1) * 2), "r"(w)
+                         : "memory");
+          }
+          __syncwarp();
+#pragma unroll
+          for (int r4 = 0; r4 < GM_ECOL / 8; ++r4) {
+            const int row = 8 * r4 + (lane >> 2);
+            const uint4 d = lds128(stg + row * 64 + (lane & 3) * 16);
+            if (ok && c0 + row < it.n) *reinterpret_cast<uint4*>(obase + (long long)(c0 + row) * a.out_ld) = d;
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(lead_accempty + 8u * buf);
+      if (++buf == 2) { buf = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while the pair's MMAs or remote arrivals may touch it
+  if (warp == GM_MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc2(tmem, GM_TMEM_COLS);
+  }
+  cluster_sync();
+}
+
 size_t ffn_gemm_ws_bytes(int, int, int, int, int) { return 0; }
 
 // ---------------------------------------------------------------- host side
@@ -573,13 +1116,56 @@ static cudaError_t gm_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
   return cudaGetLastError();
 }
 
+// CTA-pair launch: clusters of 2, as many as can be resident at once (persistent).
+// Returns cudaErrorNotSupported when no cluster of 2 fits, so that the caller can fall
+// back to the single-CTA kernel.
+template <int QT, int MODE, class Tab>
+static cudaError_t gp_launch(const GemmArgs& a, const Tab& tab, const CUtensorMap& map, cudaStream_t st) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorUnknown;
+  auto kern = gemm_pair_kernel<QT, MODE, Tab>;
+  constexpr size_t smem = gp_smem_bytes<QT>();
+  cudaError_t err = set_smem_limit<gemm_pair_kernel<QT, MODE, Tab>>(smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(di->sm_count & ~1));
+  cfg.blockDim = dim3(GM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters[2][2][5] = {};  // per (table, mode, format): resident clusters
+  int& mc = max_clusters[std::is_same<Tab, GmWithTable>::value][MODE][QT];
+  if (mc == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      return cudaErrorNotSupported;
+    }
+    mc = n;
+  }
+  cfg.gridDim = dim3((unsigned)(2 * std::min(mc, di->sm_count / 2)));
+  return cudaLaunchKernelEx(&cfg, kern, a, tab, map);
+}
+
+// Which kernel runs the prefill FFN: CTA pairs (1) or single CTAs (0).
+#ifndef FTMOE_GM_PAIR
+#define FTMOE_GM_PAIR 1
+#endif
+
 template <int QT, class Tab>
 static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
+  const bool pair = FTMOE_GM_PAIR != 0;
   CUtensorMap xmap, hmap;
   if (!make_act_map(&xmap, pb.x, pb.T, pb.H, 1) ||
-      !make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, GM_TOK))
+      !make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, pair ? GP_TOKH : GM_TOK))
     return cudaErrorNotSupported;
   GemmArgs a{};
   a.offsets = pb.offsets;
@@ -600,6 +1186,7 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   a.S = slabs_of(pb.H);
   a.nrows = pb.I;
   a.up_row0 = pb.I;
+  a.f_step = GM_ROWS;
   a.ft_per_expert = (pb.I + GM_ROWS - 1) / GM_ROWS;
   a.rec_total = (long long)records_bytes_per_expert(pb.qtype, 2 * pb.I, pb.H);
   GemmArgs d = a;
@@ -615,8 +1202,18 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   d.S = slabs_of(pb.I);
   d.nrows = pb.H;
   d.up_row0 = 0;
-  d.ft_per_expert = (pb.H + GM_ROWS - 1) / GM_ROWS;
+  d.f_step = pair ? 2 * GM_ROWS : GM_ROWS;
+  d.ft_per_expert = (pb.H + d.f_step - 1) / d.f_step;
   d.rec_total = (long long)records_bytes_per_expert(pb.qtype, pb.H, pb.I);
+  if (pair) {
+    cudaError_t err = gp_launch<QT, 0>(a, tab, xmap, st);
+    if (err == cudaSuccess) err = gp_launch<QT, 1>(d, tab, hmap, st);
+    if (err != cudaErrorNotSupported) return err;
+    // no pair fits: the single-CTA kernel with its own tensor map and slices
+    if (!make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, GM_TOK)) return cudaErrorNotSupported;
+    d.f_step = GM_ROWS;
+    d.ft_per_expert = (pb.H + GM_ROWS - 1) / GM_ROWS;
+  }
   cudaError_t err = gm_launch<QT, 0>(a, tab, xmap, st);
   if (err != cudaSuccess) return err;
   return gm_launch<QT, 1>(d, tab, hmap, st);

@@ -157,6 +157,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // mbarrier try_wait that lets the hardware suspend the thread for up to `hint_ns`
 // while the phase is incomplete, instead of returning at once (no issue slots spent
 // spinning).  Returns whether the phase completed.
+// Longest suspension of one try_wait before the wait loop looks at its abort flag and
+// clock again (overridable at build time for sweeps).
+#ifndef FTMOE_WAIT_HINT_NS
+#define FTMOE_WAIT_HINT_NS 20000u
+#endif
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
@@ -176,7 +181,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, FTMOE_WAIT_HINT_NS)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;

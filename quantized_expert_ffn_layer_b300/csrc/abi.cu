@@ -41,7 +41,7 @@ bool tke_ok(int T, int k, int E) {
 
 // Workspace carve-up shared by ftmoe_expert_ffn and ftmoe_layer.
 // Workspace of the FFN: [gemv scratch (zero region first; 0 bytes: the GEMV's split
-// reductions meet in shared memory)][h_act][gemm scratch].
+// reductions meet in shared memory)][h_act][gemm scratch: x rows in the permuted order].
 struct FfnWs {
   void* gemv_ws;
   size_t gemv_zero_bytes;

@@ -581,7 +581,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 //     (t < 16) hold the gate row and 32q + 16 + t the up row of the same feature, so one
 //     shuffle brings g and u together in the epilogue;
 //   down item: (expert, 256 rows of H, <= 256 tokens); CTA r decodes rows f0 + 128 r ...
-// Roles per CTA as in the single-CTA kernel; the first CTA (rank 0) issues every MMA.
+// Roles per CTA as in the single-CTA kernel, except that the gate/up token rows come, like
+// h for down, as TMA boxes from x_perm, the x rows written once in the permuted order by
+// gather_rows_kernel: a gather of 128-byte rows through cp.async from every stage of
+// every feature slice is limited by the L1's outstanding misses, and the TMA's row-gather
+// form by its copy rate.  The first CTA (rank 0) issues every MMA.
 // Its "operands ready" barrier counts the converter warps of both CTAs (and, for down,
 // both token warps, after their TMA box has landed); each MMA stage's commit arrives on
 // the stage's "free" barrier in both CTAs, and the accumulator barriers likewise.
@@ -591,23 +595,33 @@ constexpr int GP_STAGE = GM_A_TILE + GP_B_TILE;
 #ifndef FTMOE_GP_NS
 #define FTMOE_GP_NS 5
 #endif
-#ifndef FTMOE_GP_NR
-#define FTMOE_GP_NR 4
+// Converter warps of the pair kernel: GP_GROUPS groups of 8 that take every GP_GROUPS-th
+// stage, so that the latency chains of consecutive stages' decodes overlap.  They share
+// the operand ring safely while GP_GROUPS <= NS: a group reaching stage t has seen the
+// MMAs of stage t - GP_GROUPS - NS complete, hence those of t - 2 NS, so the slot's
+// barrier is at most one phase behind the one it waits for.
+#ifndef FTMOE_GP_GROUPS
+#define FTMOE_GP_GROUPS 2
 #endif
-// The converter warps form two groups of 8 that take alternate stages, so that the
-// latency chain of one stage's decode overlaps the other's.
-constexpr int GP_GROUP_WARPS = GM_CONV_WARPS / 2;
+constexpr int GP_GROUP_WARPS = 8;
+constexpr int GP_GROUPS = FTMOE_GP_GROUPS;
+constexpr int GP_CONV_WARPS = GP_GROUPS * GP_GROUP_WARPS;
+constexpr int GP_THREADS = (GM_CONV0 + GP_CONV_WARPS) * 32;
 // Arrivals on the first CTA's operand barrier per stage, from each CTA: the converting
-// group and the token-row warps (gate/up: the two gathering warps; down: warp 7 once the
-// TMA box has landed).  The second CTA's arrive remotely.
-template <int MODE>
-constexpr int gp_share() { return GP_GROUP_WARPS + (MODE == 0 ? 2 : 1); }
+// group and warp 7 once the stage's token rows have landed.  The second CTA's arrive
+// remotely.
+constexpr int GP_SHARE = GP_GROUP_WARPS + 1;
 template <int QT>
 struct GpCfg {
   static constexpr int NS = FTMOE_GP_NS;  // operand stages
-  static constexpr int NR = FTMOE_GP_NR;  // raw-record stages
-  static constexpr int AHEAD = 2;         // gate/up token rows gathered this many stages ahead
-  static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES && AHEAD < NS, "ring depth");
+  // Raw-record stages: a private ring of RPG slots per converter group, which the group
+  // consumes strictly in order.  (With one ring shared by groups that take stages in
+  // turn, a group could wait on a slot two phases ahead of the slot's barrier, and a
+  // parity wait cannot tell that phase from the one completed two uses earlier.)
+  // MXFP8's records are twice as large.
+  static constexpr int RPG = QT == FTMOE_MXFP8 ? 2 : (GP_GROUPS == 2 ? 4 : 3);
+  static constexpr int NR = GP_GROUPS * RPG;
+  static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES && GP_GROUPS <= NS, "ring depth");
   static constexpr int NREC = 8;          // records per stage (128 rows)
   static constexpr int RAW_STAGE = NREC * rec_bytes(QT);
 };
@@ -618,6 +632,13 @@ constexpr size_t gp_smem_bytes() {
 }
 static_assert(gp_smem_bytes<FTMOE_Q4_0>() <= 227 * 1024 && gp_smem_bytes<FTMOE_MXFP8>() <= 227 * 1024,
               "shared memory per CTA");
+// Raw-record slot and phase parity of stage t (the j-th stage of group t % GP_GROUPS).
+template <int QT>
+__device__ __forceinline__ void gp_raw_slot(int t, int& slot, uint32_t& parity) {
+  const int g = t % GP_GROUPS, j = t / GP_GROUPS;
+  slot = g * GpCfg<QT>::RPG + j % GpCfg<QT>::RPG;
+  parity = (uint32_t)(j / GpCfg<QT>::RPG) & 1u;
+}
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -713,7 +734,7 @@ __device__ __forceinline__ int gp_record_row(const GmItem& it, int ri, uint32_t 
 }
 
 template <int QT, int MODE, class Tab>
-__global__ void __launch_bounds__(GM_THREADS, 1)
+__global__ void __launch_bounds__(GP_THREADS, 1)
     gemm_pair_kernel(const GemmArgs a, const __grid_constant__ Tab tab,
                      const __grid_constant__ CUtensorMap act_map) {
   using C = GpCfg<QT>;
@@ -733,7 +754,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&tl.a_full[s], 2 * gp_share<MODE>());
+      mbar_init(&tl.a_full[s], 2 * GP_SHARE);
       mbar_init(&tl.b_full[s], 1);
       mbar_init(&tl.empty[s], 1);
     }
@@ -784,8 +805,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 
   if (warp == GM_RAW_WARP) {
     // ------------------------------------------------------------ raw weight records
-    int rslot = 0;
-    uint32_t rphase = 0;
+    int t = 0;  // stage number in this pair's sequence
     for (int i = pair; i < nitems; i += npairs) {
       const GmItem it = gm_item<MODE>(i, a, tl.citem);
       bool rok = false;
@@ -798,84 +818,26 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int nrow = gp_record_row<MODE>(nx, lane, rank, a, nok);
         if (nok) prefetch_l2(tab.get(nx.e, a) + (long long)(nrow / 16) * a.S * RB, (uint32_t)(a.S * RB));
       }
-      for (int kb = 0; kb < a.S; ++kb) {
+      for (int kb = 0; kb < a.S; ++kb, ++t) {
+        int rslot;
+        uint32_t rphase;
+        gp_raw_slot<QT>(t, rslot, rphase);
         if (!gm_wait<GM_R_RAW>(&tl.raw_empty[rslot], rphase ^ 1u, abort_flag, a.status)) break;
         if (lane == 0) mbar_arrive_expect_tx(&tl.raw_full[rslot], (uint32_t)(nrec * RB));
         __syncwarp();
         if (lane < C::NREC && rok)
           bulk_g2s(base + C::NS * GP_STAGE + rslot * C::RAW_STAGE + lane * RB, rec0 + (long long)kb * RB, RB,
                    &tl.raw_full[rslot]);
-        if (++rslot == C::NR) { rslot = 0; rphase ^= 1u; }
       }
       if (*abort_flag) break;
-    }
-  } else if (MODE == 0 && (warp == GM_TOK_WARP || warp == GM_TOK_WARP + 1)) {
-    // ------------------------------------------------------------ token rows, gate/up
-    // this CTA's half of the item's x rows, gathered through the permutation with
-    // cp.async AHEAD stages ahead; a stage is reported to the first CTA's operand barrier
-    // once its copies have landed.  Thread gt copies 16-byte chunk (gt & 7) of B rows
-    // (gt >> 3) + 8 r.
-    const int gt = tid - GM_TOK_WARP * 32;
-    constexpr int GR = GP_TOKH * 8 / 64;  // rows per thread
-    const int ch = gt & 7;
-    const uint16_t* rowp[GR];
-    int slot = 0, done_slot = 0, inflight = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int i = pair; i < nitems && ok; i += npairs) {
-      const GmItem it = gm_item<MODE>(i, a, tl.citem);
-      const int half = max(16, (it.n + 15) & ~15) / 2;
-#pragma unroll
-      for (int r = 0; r < GR; ++r) {
-        const int rr = (gt >> 3) + 8 * r;
-        const int tk = (int)rank * half + rr;  // token of the item held in B row rr
-        rowp[r] = nullptr;
-        if (rr < half && tk < it.n) {
-          const long long ar = row_token(a.sorted_pair, it.r0 + tk, a.k, a.T, a.status);
-          rowp[r] = a.act + ar * a.act_ld + ch * 8;
-        }
-      }
-      for (int kb = 0; kb < a.S; ++kb) {
-        if (!gm_wait<GM_R_TOK>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bt = base_addr + slot * GP_STAGE + GM_A_TILE;
-        const bool kok = kb * 64 + ch * 8 < a.K;  // beyond K: zeros
-#pragma unroll
-        for (int r = 0; r < GR; ++r) {
-          if (rowp[r]) {
-            const int rr = (gt >> 3) + 8 * r;
-            cp_async16(bt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) * 16),
-                       kok ? rowp[r] + kb * 64 : rowp[r], kok ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        if (++slot == C::NS) { slot = 0; phase ^= 1u; }
-        if (++inflight > C::AHEAD) {
-          cp_async_wait<C::AHEAD>();
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) gp_arrive_ready(tl.a_full, done_slot, rank);
-          if (++done_slot == C::NS) done_slot = 0;
-          --inflight;
-        }
-      }
-      if (*abort_flag) break;
-    }
-    cp_async_wait<0>();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    for (; inflight > 0 && ok && !*abort_flag; --inflight) {
-      if (lane == 0) gp_arrive_ready(tl.a_full, done_slot, rank);
-      if (++done_slot == C::NS) done_slot = 0;
     }
   } else if (warp == GM_TOK_WARP || warp == GM_TOK_WARP + 1) {
-    // ------------------------------------------------------------ token rows, down projection
-    // this CTA's half of the item's h rows: one 64 x 128 TMA box per stage, issued by
-    // warp 6 as soon as the stage is free; warp 7 reports each landed box to the first
-    // CTA's operand barrier, so that several boxes stay in flight
-    if (MODE == 1) {
+    // ------------------------------------------------------------ token rows
+    // this CTA's half of the item's rows of x_perm (gate/up) or h (down), contiguous in
+    // the permuted order: one 64 x 128 TMA box per stage, issued by warp 6 as soon as the
+    // stage is free; warp 7 reports each landed box to the first CTA's operand barrier,
+    // so that several boxes stay in flight
+    {
       const bool issuer = warp == GM_TOK_WARP;
       int slot = 0;
       uint32_t phase = 0;
@@ -901,8 +863,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else if (warp >= GM_CONV0) {
     // ------------------------------------------------------------ converters
-    // group cw / 8 converts the stages of its parity; in a stage, warp cw % 8 converts
-    // records 2 (cw % 4) + {0, 1} (half-warps), quantization block (cw / 4) % 2
+    // group cw / 8 converts stages t with t % GP_GROUPS == group; in a stage, warp cw % 8
+    // converts records 2 (cw % 4) + {0, 1} (half-warps), quantization block (cw / 4) % 2
     const int ct = tid - GM_CONV0 * 32;
     const int cw = ct >> 5;
     const int grp = cw / GP_GROUP_WARPS;
@@ -915,9 +877,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       bool rok;
       gp_record_row<MODE>(it, ri, rank, a, rok);
       for (int kb = 0; kb < a.S; ++kb, ++t) {
-        if ((t & 1) != grp) continue;
-        const int slot = t % C::NS, rslot = t % C::NR;
-        const uint32_t phase = (uint32_t)(t / C::NS) & 1u, rphase = (uint32_t)(t / C::NR) & 1u;
+        if (t % GP_GROUPS != grp) continue;
+        const int slot = t % C::NS;
+        const uint32_t phase = (uint32_t)(t / C::NS) & 1u;
+        int rslot;
+        uint32_t rphase;
+        gp_raw_slot<QT>(t, rslot, rphase);
         if (!gm_wait<GM_R_CONV>(&tl.empty[slot], phase ^ 1u, abort_flag, a.status)) break;
         if (!gm_wait<GM_R_CONV>(&tl.raw_full[rslot], rphase, abort_flag, a.status)) break;
         if (rok) {
@@ -1073,7 +1038,24 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   cluster_sync();
 }
 
-size_t ffn_gemm_ws_bytes(int, int, int, int, int) { return 0; }
+// x rows in the permuted order: xp[r][:] = x[token of permuted row r][:], one warp per
+// row, 16-byte vectors (H is a multiple of 32).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x, int H,
+                                                          const int32_t* __restrict__ sorted_pair, int k, int T,
+                                                          int P, uint16_t* __restrict__ xp, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * 8;
+  const int vecs = H / 8;
+  for (int r = (int)(blockIdx.x * 8 + (threadIdx.x >> 5)); r < P; r += nwarps) {
+    const long long t = row_token(sorted_pair, r, k, T, status);
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (long long)r * H);
+    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+// Scratch of the grouped GEMM: x_perm, bf16 [T * k][H].
+size_t ffn_gemm_ws_bytes(int T, int k, int, int H, int) { return (size_t)T * k * H * 2; }
 
 // ---------------------------------------------------------------- host side
 namespace {
@@ -1129,7 +1111,7 @@ static cudaError_t gp_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(di->sm_count & ~1));
-  cfg.blockDim = dim3(GM_THREADS);
+  cfg.blockDim = dim3(GP_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1159,13 +1141,16 @@ static cudaError_t gp_launch(const GemmArgs& a, const Tab& tab, const CUtensorMa
 #endif
 
 template <int QT, class Tab>
-static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream_t st) {
+static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, void* ws, size_t ws_bytes,
+                                cudaStream_t st) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorUnknown;
-  const bool pair = FTMOE_GM_PAIR != 0;
-  CUtensorMap xmap, hmap;
+  uint16_t* xperm = static_cast<uint16_t*>(ws);
+  const bool pair = FTMOE_GM_PAIR != 0 && xperm && ws_bytes >= (size_t)pb.P * pb.H * 2;
+  CUtensorMap xmap, hmap, xpmap;
   if (!make_act_map(&xmap, pb.x, pb.T, pb.H, 1) ||
-      !make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, pair ? GP_TOKH : GM_TOK))
+      !make_act_map(&hmap, pb.h_act, (long long)pb.P, pb.I, pair ? GP_TOKH : GM_TOK) ||
+      (pair && !make_act_map(&xpmap, xperm, (long long)pb.P, pb.H, GP_TOKH)))
     return cudaErrorNotSupported;
   GemmArgs a{};
   a.offsets = pb.offsets;
@@ -1206,7 +1191,10 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   d.ft_per_expert = (pb.H + d.f_step - 1) / d.f_step;
   d.rec_total = (long long)records_bytes_per_expert(pb.qtype, pb.H, pb.I);
   if (pair) {
-    cudaError_t err = gp_launch<QT, 0>(a, tab, xmap, st);
+    const int gblocks = std::max(1, std::min((pb.P + 7) / 8, di->sm_count * 8));
+    gather_rows_kernel<<<gblocks, 256, 0, st>>>(pb.x, pb.H, pb.sorted_pair, pb.k, pb.T, pb.P, xperm, di->status);
+    cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) err = gp_launch<QT, 0>(a, tab, xpmap, st);
     if (err == cudaSuccess) err = gp_launch<QT, 1>(d, tab, hmap, st);
     if (err != cudaErrorNotSupported) return err;
     // no pair fits: the single-CTA kernel with its own tensor map and slices
@@ -1219,21 +1207,21 @@ static cudaError_t gm_launch_qt(const FfnProblem& pb, const Tab& tab, cudaStream
   return gm_launch<QT, 1>(d, tab, hmap, st);
 }
 
-cudaError_t launch_ffn_gemm(const FfnProblem& pb, void*, size_t, cudaStream_t st) {
+cudaError_t launch_ffn_gemm(const FfnProblem& pb, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (pb.E > GM_MAX_E) return cudaErrorNotSupported;
   if (pb.table) {
     GmWithTable t;
     t.t = *pb.table;
-    return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
-           : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, st)
-           : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, st)
-                                     : gm_launch_qt<FTMOE_MXFP8>(pb, t, st);
+    return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_bytes, st)
+           : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_bytes, st)
+           : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, ws, ws_bytes, st)
+                                     : gm_launch_qt<FTMOE_MXFP8>(pb, t, ws, ws_bytes, st);
   }
   GmNoTable t;
-  return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, st)
-         : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, st)
-         : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, st)
-                                   : gm_launch_qt<FTMOE_MXFP8>(pb, t, st);
+  return pb.qtype == FTMOE_Q4_0    ? gm_launch_qt<FTMOE_Q4_0>(pb, t, ws, ws_bytes, st)
+         : pb.qtype == FTMOE_MXFP4 ? gm_launch_qt<FTMOE_MXFP4>(pb, t, ws, ws_bytes, st)
+         : pb.qtype == FTMOE_NVFP4 ? gm_launch_qt<FTMOE_NVFP4>(pb, t, ws, ws_bytes, st)
+                                   : gm_launch_qt<FTMOE_MXFP8>(pb, t, ws, ws_bytes, st);
 }
 
 }  // namespace ftmoe

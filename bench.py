@@ -34,6 +34,10 @@ sys.path.insert(0, ROOT)
 from synth import CONFIGS, gen_logits, make_layer  # noqa: E402
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# B300 nominal figures, reported beside the measured peaks: HBM3e 7.7 TB/s, dense bf16
+# 2.25 PFLOP/s.
+NOMINAL_HBM_GBS = 7700.0
+NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -840,17 +844,21 @@ def ffn_roofline(L, U, ffn_ms, pk, pk_kind, workload, path="auto"):
                 "gemm_decode_kernel x2 (tcgen05, A in tensor memory; gate/up+SwiGLU, down)")
         return {"bound": "hbm", "kernel": name, "path": used,
                 "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "frac_nominal": ach / NOMINAL_HBM_GBS,
                 "peak_kind": f"{pk_kind} hbm_gbs (copy)",
                 "traffic": recorded_traffic("expert_ffn_" + used, workload),
                 "alg_bytes_per_launch": alg, "ms_per_launch": ffn_ms, "unique_experts": U}
     flops = 2.0 * P * 3 * H * I
     peak = float(pk["bf16_tflops"])
     ach = flops / (ffn_ms / 1e3) / 1e12
-    return {"bound": "tensor", "kernel": "gemm_ffn_kernel x2 (tcgen05 kind::f16; gate/up+SwiGLU, down)",
+    return {"bound": "tensor",
+            "kernel": "gather_rows_kernel + gemm_pair_kernel x2 (tcgen05 kind::f16 on CTA pairs; gate/up+SwiGLU, down)",
             "path": used,
             "operand": f"bf16 decoded from the {L.qtype} bank in shared memory (kind::f16 on every "
-                       "format, so the bf16 peak is the denominator; no block-scaled FP4 / FP8 MMA)",
+                       "format, so the bf16 peak is the denominator; MXFP4 here is bf16-emulated: "
+                       "no block-scaled FP4 / FP8 MMA is built)",
             "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+            "frac_nominal": ach / NOMINAL_BF16_TFLOPS,
             "peak_kind": f"{pk_kind} bf16_tflops (burst; the FFN is timed alone)",
             "traffic": recorded_traffic("expert_ffn_gemm", workload),
             "alg_flops_per_launch": flops, "ms_per_launch": ffn_ms, "unique_experts": U}

@@ -600,10 +600,12 @@ constexpr int GP_STAGE = GM_A_TILE + GP_B_TILE;
 // the operand ring safely while GP_GROUPS <= NS: a group reaching stage t has seen the
 // MMAs of stage t - GP_GROUPS - NS complete, hence those of t - 2 NS, so the slot's
 // barrier is at most one phase behind the one it waits for.
+// A group converts a stage's 8 records with 8 warps (each thread 2 of a record's 4
+// steps) or, with FTMOE_GP_NSTEP = 4, with 4 warps (each half-warp a whole record).
+constexpr int GP_GROUP_WARPS = FTMOE_GP_NSTEP == 4 ? 4 : 8;
 #ifndef FTMOE_GP_GROUPS
-#define FTMOE_GP_GROUPS 2
+#define FTMOE_GP_GROUPS (16 / GP_GROUP_WARPS)
 #endif
-constexpr int GP_GROUP_WARPS = 8;
 constexpr int GP_GROUPS = FTMOE_GP_GROUPS;
 constexpr int GP_CONV_WARPS = GP_GROUPS * GP_GROUP_WARPS;
 constexpr int GP_THREADS = (GM_CONV0 + GP_CONV_WARPS) * 32;
@@ -619,7 +621,7 @@ struct GpCfg {
   // turn, a group could wait on a slot two phases ahead of the slot's barrier, and a
   // parity wait cannot tell that phase from the one completed two uses earlier.)
   // MXFP8's records are twice as large.
-  static constexpr int RPG = QT == FTMOE_MXFP8 ? 2 : (GP_GROUPS == 2 ? 4 : 3);
+  static constexpr int RPG = QT == FTMOE_MXFP8 ? (GP_GROUPS > 2 ? 1 : 2) : (GP_GROUPS > 2 ? 2 : 4);
   static constexpr int NR = GP_GROUPS * RPG;
   static_assert(NS <= GM_MAX_STAGES && NR <= GM_MAX_STAGES && GP_GROUPS <= NS, "ring depth");
   static constexpr int NREC = 8;          // records per stage (128 rows)
@@ -863,13 +865,14 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     }
   } else if (warp >= GM_CONV0) {
     // ------------------------------------------------------------ converters
-    // group cw / 8 converts stages t with t % GP_GROUPS == group; in a stage, warp cw % 8
-    // converts records 2 (cw % 4) + {0, 1} (half-warps), quantization block (cw / 4) % 2
+    // group cw / GP_GROUP_WARPS converts stages t with t % GP_GROUPS == group; in a stage,
+    // warp w = cw % GP_GROUP_WARPS converts records 2 (w % 4) + {0, 1} (half-warps), whole
+    // (4 warps a group) or quantization block w / 4 (8 warps a group)
     const int ct = tid - GM_CONV0 * 32;
     const int cw = ct >> 5;
     const int grp = cw / GP_GROUP_WARPS;
     const int ri = 2 * (cw & 3) + (lane >> 4);
-    const int jsel = (cw >> 2) & 1;
+    const int jsel = ((cw % GP_GROUP_WARPS) >> 2) & 1;
     const int g = (lane & 15) >> 1, m = lane & 1;
     int t = 0;  // stage number in this pair's sequence
     for (int i = pair; i < nitems; i += npairs) {
@@ -888,7 +891,8 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         if (rok) {
           const uint32_t rec = rawring + rslot * C::RAW_STAGE + ri * RB;
           const uint32_t st_base = base_addr + slot * GP_STAGE;
-          if (jsel) convert_record_operand<QT, 2, 2>(rec, st_base, ri, g, m);
+          if (FTMOE_GP_NSTEP == 4) convert_record_operand<QT, 4, 0>(rec, st_base, ri, g, m);
+          else if (jsel) convert_record_operand<QT, 2, 2>(rec, st_base, ri, g, m);
           else convert_record_operand<QT, 2, 0>(rec, st_base, ri, g, m);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -51,6 +51,12 @@ __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
 }
 
 // ---------------------------------------------------------------- prefill A tile
+// Steps (of 16 elements) one converter thread of the prefill GEMM decodes per record
+// and stage: 4 (a half-warp converts a whole record) or 2 (half a record).  The
+// operand check (operand_check.cu) converts with the same span.
+#ifndef FTMOE_GP_NSTEP
+#define FTMOE_GP_NSTEP 4
+#endif
 // A-tile row order: weight row r of a 16-row record is stored at tile row sigma(r)
 // (rows 0..3 -> 0,2,4,6, rows 4..7 -> 1,3,5,7, and the same +8 for rows 8..15), so
 // that the converter stores of a quarter-warp fall on 8 different 16-byte bank groups.
@@ -135,17 +141,19 @@ __device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi,
 // One converter thread's share of a record in shared memory.  Record lanes 4g + 2m (A)
 // and 4g + 2m + 1 (B) hold elements 8m..8m+7 of each 16-element step j of rows g and
 // g + 8 (A: elements 8m..8m+3, B: 8m+4..8m+7).  The thread decodes NSTEP steps starting
-// at J0 (NSTEP = 2: quantization block J0 / 2; NSTEP = 1: one step) of both rows into the
-// A tile at `tile` (128 rows of 64 bf16, 128-byte swizzle), record row group rg.  Lane
-// pairs (m = 0, 1) share the scale conversions through one shuffle, so all 32 lanes of
-// the warp must call it together.  The two 16-byte code loads are issued in an order
-// that depends on (g >> 1) & 1 so that each quarter-warp reads 8 different bank groups.
+// at J0 (NSTEP = 1, 2 or 4; a span of 2 or 4 starts on a quantization block) of both
+// rows into the A tile at `tile` (128 rows of 64 bf16, 128-byte swizzle), record row
+// group rg.  Lane pairs (m = 0, 1) share the scale conversions through one shuffle, so
+// all 32 lanes of the warp must call it together.  The two 16-byte code loads are issued
+// in an order that depends on (g >> 1) & 1 so that each quarter-warp reads 8 different
+// bank groups.
 template <int QT, int NSTEP, int J0>
 __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t tile, int rg, int g,
                                                         int m) {
-  // scales per thread: one per 32-element block (Q4_0, MXFP4: both steps share it), one
+  static_assert(NSTEP == 1 || (NSTEP == 2 && J0 % 2 == 0) || (NSTEP == 4 && J0 == 0), "step span");
+  // scales per thread: one per 32-element block (Q4_0, MXFP4: two steps share one), one
   // per step for NVFP4's 16-element blocks
-  constexpr int NSC = QT == FTMOE_NVFP4 ? NSTEP : 1;
+  constexpr int NSC = QT == FTMOE_NVFP4 ? NSTEP : (NSTEP + 1) / 2;
   const int sw = (g >> 1) & 1;
   const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
   const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
@@ -158,7 +166,7 @@ __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t t
   uint32_t sh0[NSC], sl0[NSC], sh1[NSC], sl1[NSC];
 #pragma unroll
   for (int u = 0; u < NSC; ++u) {
-    const int idx = QT == FTMOE_NVFP4 ? (g * 4 + J0 + u) * 2 + m : (g * 2 + (J0 >> 1)) * 2 + m;
+    const int idx = QT == FTMOE_NVFP4 ? (g * 4 + J0 + u) * 2 + m : (g * 2 + (J0 >> 1) + u) * 2 + m;
     const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
     const uint32_t w = lds32(rec + REC_CODE_BYTES + (byte & ~3));
     const uint32_t sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
@@ -176,7 +184,7 @@ __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t t
 #pragma unroll
   for (int s = 0; s < NSTEP; ++s) {
     const int j = J0 + s;
-    const int u = NSC > 1 ? s : 0;
+    const int u = QT == FTMOE_NVFP4 ? s : (j >> 1) - (J0 >> 1);
     const uint32_t A = wa[j], Bw = wb[j];
     const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;
     if (QT == FTMOE_Q4_0) {
@@ -202,19 +210,27 @@ __device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t t
 template <int NSTEP, int J0>
 __device__ __forceinline__ void convert_record_swizzled_fp8(uint32_t rec, uint32_t tile, int rg, int g,
                                                             int m) {
+  static_assert(NSTEP == 1 || (NSTEP == 2 && J0 % 2 == 0) || (NSTEP == 4 && J0 == 0), "step span");
+  constexpr int NB = (NSTEP + 1) / 2;  // 32-element blocks spanned
   const uint32_t la = rec + (4 * g + 2 * m) * 32;
   const int T0 = rg * 16 + gm_sigma(g);
   const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
   const uint32_t row1 = row0 + 1024;
   const uint32_t ph = (uint32_t)(T0 & 7);
-  const uint32_t sw = lds32(rec + 1024 + (g * 2 + (J0 >> 1)) * 2 - ((g * 2 + (J0 >> 1)) * 2 & 3));
-  const int sb = ((g * 2 + (J0 >> 1)) * 2) & 3;
-  uint32_t s0h, s0l, s1h, s1l;
-  row_scale<FTMOE_MXFP4>((sw >> (8 * sb)) & 0xFFu, s0h, s0l);        // row g
-  row_scale<FTMOE_MXFP4>((sw >> (8 * (sb + 1))) & 0xFFu, s1h, s1l);  // row g + 8
+  // E8M0 scales [g][b][h]: rows g (h = 0) and g + 8 (h = 1) of each spanned block
+  uint32_t s0hb[NB], s1hb[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int byte = (g * 2 + (J0 >> 1) + b) * 2;
+    const uint32_t sw = lds32(rec + 1024 + (byte & ~3));
+    uint32_t l0, l1;
+    row_scale<FTMOE_MXFP4>((sw >> (8 * (byte & 3))) & 0xFFu, s0hb[b], l0);        // row g
+    row_scale<FTMOE_MXFP4>((sw >> (8 * ((byte & 3) + 1))) & 0xFFu, s1hb[b], l1);  // row g + 8
+  }
 #pragma unroll
   for (int s = 0; s < NSTEP; ++s) {
     const int j = J0 + s;
+    const uint32_t s0h = s0hb[(j >> 1) - (J0 >> 1)], s1h = s1hb[(j >> 1) - (J0 >> 1)];
     const uint2 A = lds64(la + 8 * j);        // (row g, row g + 8) elements 8m..8m+3
     const uint2 B = lds64(la + 32 + 8 * j);   // elements 8m+4..8m+7
     const uint32_t off = (((uint32_t)(2 * j + m)) ^ ph) * 16;

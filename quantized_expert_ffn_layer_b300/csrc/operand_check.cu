@@ -13,9 +13,10 @@ namespace ftmoe {
 constexpr int OC_ROWS = 128;  // A-tile rows of the prefill GEMM
 
 // One CTA per (expert, 128-row tile, 64-element slab): the tile's (up to) 8 records are
-// copied to shared memory, 8 warps convert them exactly as the prefill GEMM's gate/up
-// converters do (warp w: records 2 (w / 2) + {0, 1}, quantization block w % 2), and the
-// swizzled A tile is read back row by row (tile row -> record row via sigma^-1).
+// copied to shared memory, converted exactly as the prefill GEMM's converters do
+// (FTMOE_GP_NSTEP = 4: warp w < 4 converts records 2w + {0, 1} whole; 2: warp w
+// records 2 (w / 2) + {0, 1}, quantization block w % 2), and the swizzled A tile is
+// read back row by row (tile row -> record row via sigma^-1).
 template <int QT>
 __global__ void __launch_bounds__(256) operand_prefill_kernel(const uint8_t* __restrict__ tiles,
                                                               uint16_t* __restrict__ out, int E,
@@ -42,12 +43,17 @@ __global__ void __launch_bounds__(256) operand_prefill_kernel(const uint8_t* __r
   }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
-  const int ri = 2 * (warp >> 1) + (lane >> 4);
   const int g = (lane & 15) >> 1, m = lane & 1;
-  const uint32_t rec = smem_u32(raw) + ri * RB;
   const uint32_t tbase = smem_u32(tile);
-  if (warp & 1) convert_record_operand<QT, 2, 2>(rec, tbase, ri, g, m);
-  else convert_record_operand<QT, 2, 0>(rec, tbase, ri, g, m);
+  if (FTMOE_GP_NSTEP == 4) {
+    const int ri = 2 * warp + (lane >> 4);
+    if (warp < 4) convert_record_operand<QT, 4, 0>(smem_u32(raw) + ri * RB, tbase, ri, g, m);
+  } else {
+    const int ri = 2 * (warp >> 1) + (lane >> 4);
+    const uint32_t rec = smem_u32(raw) + ri * RB;
+    if (warp & 1) convert_record_operand<QT, 2, 2>(rec, tbase, ri, g, m);
+    else convert_record_operand<QT, 2, 0>(rec, tbase, ri, g, m);
+  }
   __syncthreads();
   // thread t: tile row t / 2, chunks 4 (t % 2) .. +3 (8 bf16 each)
   const int Tr = tid >> 1, h = tid & 1;

@@ -89,3 +89,7 @@ def test_workspace_sizes_grow_with_the_problem(F):
     c = F.ftmoe_layer_workspace_bytes(64, 8, 128, 2048, 768, 1)  # with a shared expert
     assert 0 < a < b and c > a
     assert F.ftmoe_ffn_workspace_bytes(64, 8, 128, 2048, 768) <= a
+    # the FFN scratch holds h ([T*k][I] bf16) and, for the tensor-core prefill path, x in
+    # the permuted order ([T*k][H] bf16)
+    P = 4096 * 8
+    assert F.ftmoe_ffn_workspace_bytes(4096, 8, 128, 2048, 768) >= P * 768 * 2 + P * 2048 * 2

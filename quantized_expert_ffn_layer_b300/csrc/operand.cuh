@@ -147,69 +147,40 @@ __device__ __forceinline__ uint4 q4_scale(const uint32_t (&t)[4], uint32_t s_hi,
 // all 32 lanes of the warp must call it together.  The two 16-byte code loads are issued
 // in an order that depends on (g >> 1) & 1 so that each quarter-warp reads 8 different
 // bank groups.
-// The conversion in three phases, so that a converter can issue the shared-memory loads
-// of its next record before it decodes and stores the current one (load_share: loads
-// only; prep_share: the block scales, with one shuffle between lane pairs m = 0, 1, so
-// all 32 lanes of the warp call it together; store_share: decode and store).
 template <int QT, int NSTEP, int J0>
-struct RecShare {
+__device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t tile, int rg, int g,
+                                                        int m) {
   static_assert(NSTEP == 1 || (NSTEP == 2 && J0 % 2 == 0) || (NSTEP == 4 && J0 == 0), "step span");
   // scales per thread: one per 32-element block (Q4_0, MXFP4: two steps share one), one
   // per step for NVFP4's 16-element blocks
-  static constexpr int NSC = QT == FTMOE_NVFP4 ? NSTEP : (NSTEP + 1) / 2;
-  uint4 ca, cb;       // code words of record lanes 4g + 2m (A) and 4g + 2m + 1 (B)
-  uint32_t w[NSC];    // scale words as loaded
-  // scale of row g (sh0, sl0) and row g + 8 (sh1, sl1) as (hi, lo) bf16x2, see row_scale
-  uint32_t sh0[NSC], sl0[NSC], sh1[NSC], sl1[NSC];
-};
-
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ int share_scale_byte(int g, int m, int u) {
-  const int idx = QT == FTMOE_NVFP4 ? (g * 4 + J0 + u) * 2 + m : (g * 2 + (J0 >> 1) + u) * 2 + m;
-  return QT == FTMOE_Q4_0 ? idx * 2 : idx;
-}
-
-// The two 16-byte code loads are issued in an order that depends on (g >> 1) & 1 so
-// that each quarter-warp reads 8 different bank groups.
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ void load_share(uint32_t rec, int g, int m, RecShare<QT, NSTEP, J0>& r) {
+  constexpr int NSC = QT == FTMOE_NVFP4 ? NSTEP : (NSTEP + 1) / 2;
   const int sw = (g >> 1) & 1;
   const uint4 l1 = lds128(rec + (4 * g + 2 * m + sw) * 16);
   const uint4 l2 = lds128(rec + (4 * g + 2 * m + 1 - sw) * 16);
-  r.ca = sw ? l2 : l1;
-  r.cb = sw ? l1 : l2;
-#pragma unroll
-  for (int u = 0; u < RecShare<QT, NSTEP, J0>::NSC; ++u)
-    r.w[u] = lds32(rec + REC_CODE_BYTES + (share_scale_byte<QT, NSTEP, J0>(g, m, u) & ~3));
-}
-
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ void prep_share(int g, int m, RecShare<QT, NSTEP, J0>& r) {
-#pragma unroll
-  for (int u = 0; u < RecShare<QT, NSTEP, J0>::NSC; ++u) {
-    const int byte = share_scale_byte<QT, NSTEP, J0>(g, m, u);
-    const uint32_t sbits = QT == FTMOE_Q4_0 ? (r.w[u] >> (8 * (byte & 3))) & 0xFFFFu
-                                            : (r.w[u] >> (8 * (byte & 3))) & 0xFFu;
-    uint32_t mh, ml;  // scale of row g + 8 m (this lane); the partner lane has the other row
-    row_scale<QT>(sbits, mh, ml);
-    const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
-    const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
-    r.sh0[u] = m ? oh : mh;
-    r.sl0[u] = m ? ol : ml;
-    r.sh1[u] = m ? mh : oh;
-    r.sl1[u] = m ? ml : ol;
-  }
-}
-
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ void store_share(const RecShare<QT, NSTEP, J0>& r, uint32_t tile, int rg, int g,
-                                            int m) {
+  const uint4 ca = sw ? l2 : l1, cb = sw ? l1 : l2;
   const int T0 = rg * 16 + gm_sigma(g);  // tile row of record row g (row g + 8: T0 + 8)
   const uint32_t row0 = tile + (T0 >> 3) * 1024 + (T0 & 7) * 128;
   const uint32_t row1 = row0 + 1024;
   const uint32_t ph = (uint32_t)(T0 & 7);
-  const uint32_t wa[4] = {r.ca.x, r.ca.y, r.ca.z, r.ca.w};
-  const uint32_t wb[4] = {r.cb.x, r.cb.y, r.cb.z, r.cb.w};
+  // scale of row g + 8 m (this lane) and of the other row (partner lane)
+  uint32_t sh0[NSC], sl0[NSC], sh1[NSC], sl1[NSC];
+#pragma unroll
+  for (int u = 0; u < NSC; ++u) {
+    const int idx = QT == FTMOE_NVFP4 ? (g * 4 + J0 + u) * 2 + m : (g * 2 + (J0 >> 1) + u) * 2 + m;
+    const int byte = QT == FTMOE_Q4_0 ? idx * 2 : idx;
+    const uint32_t w = lds32(rec + REC_CODE_BYTES + (byte & ~3));
+    const uint32_t sbits = QT == FTMOE_Q4_0 ? (w >> (8 * (byte & 3))) & 0xFFFFu : (w >> (8 * (byte & 3))) & 0xFFu;
+    uint32_t mh, ml;
+    row_scale<QT>(sbits, mh, ml);
+    const uint32_t oh = __shfl_xor_sync(0xffffffffu, mh, 1);
+    const uint32_t ol = __shfl_xor_sync(0xffffffffu, ml, 1);
+    sh0[u] = m ? oh : mh;
+    sl0[u] = m ? ol : ml;
+    sh1[u] = m ? mh : oh;
+    sl1[u] = m ? ml : ol;
+  }
+  const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+  const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
   for (int s = 0; s < NSTEP; ++s) {
     const int j = J0 + s;
@@ -220,30 +191,15 @@ __device__ __forceinline__ void store_share(const RecShare<QT, NSTEP, J0>& r, ui
       uint32_t t0[4], t1[4];
       q4_pairs(A & 0x0F0F0F0Fu, Bw & 0x0F0F0F0Fu, t0);                // row g
       q4_pairs((A >> 4) & 0x0F0F0F0Fu, (Bw >> 4) & 0x0F0F0F0Fu, t1);  // row g + 8
-      sts128(row0 + off, q4_scale(t0, r.sh0[u], r.sl0[u]));
-      sts128(row1 + off, q4_scale(t1, r.sh1[u], r.sl1[u]));
+      sts128(row0 + off, q4_scale(t0, sh0[u], sl0[u]));
+      sts128(row1 + off, q4_scale(t1, sh1[u], sl1[u]));
     } else {
       const uint32_t wg = (A & 0x0F0F0F0Fu) | ((Bw & 0x0F0F0F0Fu) << 4);
       const uint32_t wg8 = ((A >> 4) & 0x0F0F0F0Fu) | (Bw & 0xF0F0F0F0u);
-      sts128(row0 + off, e2m1_scaled8(wg, r.sh0[u]));
-      sts128(row1 + off, e2m1_scaled8(wg8, r.sh1[u]));
+      sts128(row0 + off, e2m1_scaled8(wg, sh0[u]));
+      sts128(row1 + off, e2m1_scaled8(wg8, sh1[u]));
     }
   }
-}
-
-// One converter thread's share of a record in shared memory.  Record lanes 4g + 2m (A)
-// and 4g + 2m + 1 (B) hold elements 8m..8m+7 of each 16-element step j of rows g and
-// g + 8 (A: elements 8m..8m+3, B: 8m+4..8m+7).  The thread decodes NSTEP steps starting
-// at J0 (NSTEP = 1, 2 or 4; a span of 2 or 4 starts on a quantization block) of both
-// rows into the A tile at `tile` (128 rows of 64 bf16, 128-byte swizzle), record row
-// group rg; all 32 lanes of the warp call it together (see prep_share).
-template <int QT, int NSTEP, int J0>
-__device__ __forceinline__ void convert_record_swizzled(uint32_t rec, uint32_t tile, int rg, int g,
-                                                        int m) {
-  RecShare<QT, NSTEP, J0> r;
-  load_share(rec, g, m, r);
-  prep_share(g, m, r);
-  store_share(r, tile, rg, g, m);
 }
 
 // MXFP8: the same thread roles on 1056-byte records.  Thread (g, m) writes elements

@@ -228,7 +228,10 @@ typedef struct {
 /* Bytes of one expert blob (tiles of w13[e] then w2[e]). */
 size_t ftmoe_expert_blob_bytes(int qtype, int H, int I);
 
-/* Scratch for ftmoe_expert_ffn / ftmoe_layer (device, 256-byte aligned). */
+/* Scratch for ftmoe_expert_ffn / ftmoe_layer (device, 256-byte aligned, owned by the
+ * caller, contents undefined between calls): the intermediate h (bf16 [T*k][I]) and,
+ * for the tensor-core prefill path, the x rows in the permuted order (bf16 [T*k][H]);
+ * ftmoe_layer adds the routing and permutation arrays. */
 size_t ftmoe_ffn_workspace_bytes(int T, int k, int E, int H, int I);
 size_t ftmoe_layer_workspace_bytes(int T, int k, int E, int H, int I, int has_shared);
 

@@ -51,29 +51,83 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """SM clocks and throttle reasons sampled during the timed region: through NVML every
+    10 ms when the NVML binding loads (a timed region of a few tens of milliseconds then
+    still gets several samples), else nvidia-smi every 0.2 s.  Reads only."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_PERIOD_S = 0.01
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, pci_bus_id: str = None):
+        # NVML and nvidia-smi number every GPU of the machine; the PCI bus id (when given)
+        # picks the one this process's CUDA device is, whatever CUDA_VISIBLE_DEVICES says
         self.index = index
+        self.pci_bus_id = pci_bus_id
         self.rows = []
+        self.source = None
         self._stop = threading.Event()
         self._t = None
 
+    def _nvml_reader(self):
+        """A function returning one row in nvidia-smi's column order, or None."""
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+        except Exception:
+            return None
+        h = None
+        if self.pci_bus_id:
+            try:
+                h = nv.nvmlDeviceGetHandleByPciBusId(self.pci_bus_id)
+            except Exception:
+                h = None
+        if h is None:
+            try:
+                h = nv.nvmlDeviceGetHandleByIndex(self.index)
+            except Exception:
+                return None
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        bits = [getattr(nv, "nvmlClocksEventReason" + n, getattr(nv, "nvmlClocksThrottleReason" + n, d))
+                for n, d in (("HwSlowdown", 0x8), ("HwThermalSlowdown", 0x40),
+                             ("SwThermalSlowdown", 0x20), ("SwPowerCap", 0x4))]
+
+        def read():
+            sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+            mx = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+            try:
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+            except Exception:
+                pw = float("nan")
+            r = int(reasons(h))
+            act = lambda b: "Active" if r & b else "Not Active"
+            return [str(self.index), str(sm), str(mx), f"{pw:.2f}", hex(r)] + [act(b) for b in bits]
+        return read
+
+    def _smi_row(self):
+        try:
+            r = subprocess.run(["nvidia-smi", f"--id={self.pci_bus_id or self.index}", f"--query-gpu={self.Q}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                               timeout=5)
+            if r.returncode == 0 and r.stdout.strip():
+                return [s.strip() for s in r.stdout.strip().split(",")]
+        except Exception:
+            pass
+        return None
+
     def _run(self):
+        read = self._nvml_reader()
+        self.source = "nvml" if read else "nvidia-smi"
         while not self._stop.is_set():
             try:
-                r = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                    "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                                   timeout=5)
-                if r.returncode == 0 and r.stdout.strip():
-                    self.rows.append([s.strip() for s in r.stdout.strip().split(",")])
+                row = read() if read else self._smi_row()
             except Exception:
-                pass
-            self._stop.wait(0.2)
+                row = None
+            if row:
+                self.rows.append(row)
+            self._stop.wait(self.NVML_PERIOD_S if read else 0.2)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
@@ -94,7 +148,18 @@ class ClockSampler:
         reasons = sorted({names[i] for r in self.rows for i in range(4)
                           if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
         return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows),
+                "source": self.source}
+
+
+def pci_bus_id(dev):
+    """PCI bus id of a CUDA device as NVML / nvidia-smi spell it, or None."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
 
 
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
@@ -260,7 +325,7 @@ def main():
         run_large(args, world, rank, pg, dev, flush, stream, pk, pk_kind, cfg, L)
         return
 
-    clk = ClockSampler(local_rank)
+    clk = ClockSampler(local_rank, pci_bus_id(dev))
     head = measure_layer(L, dev, args.steps, args.warmup, flush, stream, pg, clk=clk)
     U = head["U"]
     T, k, E, H, I = L.T, L.k, L.E, L.H, L.I
@@ -371,7 +436,7 @@ def run_large(args, world, rank, pg, dev, flush, stream, pk, pk_kind, cfg, L):
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    clk = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clk = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")), pci_bus_id(dev))
     with clk:
         r = measure_large(dev, args.steps, args.warmup, flush, stream, pk, pk_kind, rank,
                           cpu_tokens=0 if (args.no_cpu_baseline or world > 1) else 4, L=L)

@@ -79,3 +79,48 @@ def test_every_bank_format_is_a_bench_format():
     assert set(CONFIGS["decode"]["qtypes"]) == {"q4_0", "mxfp4", "nvfp4", "mxfp8"}
     assert set(CONFIGS["prefill"]["qtypes"]) == {"q4_0", "mxfp4", "nvfp4", "mxfp8"}
     assert CONFIGS["stream"]["steps"] == 2048
+
+
+def test_clock_sampler_reads_nvml_often_and_maps_reasons(monkeypatch):
+    """The sampler takes NVML readings every 10 ms (a short timed region still gets several
+    samples) and reports the throttle reasons that were active, from a fake NVML."""
+    import sys
+    import time
+    import types
+    calls = {"n": 0}
+    fake = types.SimpleNamespace(
+        NVML_CLOCK_SM=1,
+        nvmlInit=lambda: None,
+        nvmlDeviceGetHandleByIndex=lambda i: ("gpu", i),
+        nvmlDeviceGetHandleByPciBusId=lambda b: ("gpu", b),
+        nvmlDeviceGetClockInfo=lambda h, c: 1965,
+        nvmlDeviceGetMaxClockInfo=lambda h, c: 2032,
+        nvmlDeviceGetPowerUsage=lambda h: 850000,
+        nvmlClocksEventReasonSwPowerCap=0x4, nvmlClocksEventReasonHwSlowdown=0x8,
+        nvmlClocksEventReasonSwThermalSlowdown=0x20, nvmlClocksEventReasonHwThermalSlowdown=0x40)
+
+    def reasons(h):
+        calls["n"] += 1
+        return 0x4 if calls["n"] % 2 else 0x0  # sw_power_cap on every other reading
+    fake.nvmlDeviceGetCurrentClocksEventReasons = reasons
+    monkeypatch.setitem(sys.modules, "pynvml", fake)
+    clk = bench.ClockSampler(0, "00000000:1B:00.0")
+    with clk:
+        time.sleep(0.15)
+    s = clk.summary()
+    assert s["source"] == "nvml" and s["samples"] >= 5
+    assert s["sm_mhz"] == 1965.0 and s["sm_max_mhz"] == 2032.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_falls_back_without_nvml(monkeypatch):
+    import sys
+    monkeypatch.setitem(sys.modules, "pynvml", None)  # import fails
+    clk = bench.ClockSampler(0)
+    monkeypatch.setattr(clk, "_smi_row", lambda: ["0", "2032", "2032", "800.00", "0x0",
+                                                  "Not Active", "Not Active", "Not Active", "Active"])
+    with clk:
+        import time
+        time.sleep(0.05)
+    s = clk.summary()
+    assert s["source"] == "nvidia-smi" and s["samples"] >= 1 and s["reasons"] == ["sw_power_cap"]

@@ -52,8 +52,9 @@ def peaks():
 
 class ClockSampler:
     """SM clocks and throttle reasons sampled during the timed region: through NVML every
-    10 ms when the NVML binding loads (a timed region of a few tens of milliseconds then
-    still gets several samples), else nvidia-smi every 0.2 s.  Reads only."""
+    10 ms when the NVML binding loads, else from one nvidia-smi process in its loop mode
+    every 20 ms, so that a timed region of a few tens of milliseconds still gets several
+    samples.  Reads only."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,17 +118,48 @@ class ClockSampler:
             pass
         return None
 
+    SMI_PERIOD_MS = 20
+
+    def _smi_stream(self):
+        """nvidia-smi in its own loop mode (one process, a sample every SMI_PERIOD_MS),
+        read until stop; the process is ended through its own handle."""
+        try:
+            proc = subprocess.Popen(["nvidia-smi", f"--id={self.pci_bus_id or self.index}",
+                                     f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                     "-lms", str(self.SMI_PERIOD_MS)],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return False
+        self._proc = proc
+        for line in proc.stdout:
+            row = [c.strip() for c in line.strip().split(",")]
+            if len(row) >= 9:
+                self.rows.append(row)
+            if self._stop.is_set():
+                break
+        return True
+
     def _run(self):
         read = self._nvml_reader()
-        self.source = "nvml" if read else "nvidia-smi"
-        while not self._stop.is_set():
-            try:
-                row = read() if read else self._smi_row()
-            except Exception:
-                row = None
+        if read:
+            self.source = "nvml"
+            while not self._stop.is_set():
+                try:
+                    row = read()
+                except Exception:
+                    row = None
+                if row:
+                    self.rows.append(row)
+                self._stop.wait(self.NVML_PERIOD_S)
+            return
+        self.source = "nvidia-smi"
+        if self._smi_stream():
+            return
+        while not self._stop.is_set():  # one nvidia-smi call per sample
+            row = self._smi_row()
             if row:
                 self.rows.append(row)
-            self._stop.wait(self.NVML_PERIOD_S if read else 0.2)
+            self._stop.wait(0.2)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
@@ -135,7 +167,18 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        # a region shorter than nvidia-smi's start-up still gets its first sample
+        deadline = time.time() + 2.0
+        while not self.rows and time.time() < deadline and self._t is not None and self._t.is_alive():
+            time.sleep(0.01)
         self._stop.set()
+        proc = getattr(self, "_proc", None)
+        if proc is not None:
+            try:
+                proc.terminate()
+                proc.wait(timeout=5)
+            except Exception:
+                pass
         if self._t:
             self._t.join(timeout=10)
 
@@ -147,9 +190,12 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in self.rows for i in range(4)
                           if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows),
-                "source": self.source}
+        out = {"sm_mhz": float(np.median(sm)) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows),
+               "source": self.source}
+        if getattr(self, "window", None):
+            out["window"] = self.window
+        return out
 
 
 def pci_bus_id(dev):
@@ -163,6 +209,7 @@ def pci_bus_id(dev):
 
 
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+CLOCK_PREROLL_S = 0.3
 KERNEL_SOURCES = {
     "expert_ffn_gemv": ["gemv.cu", "operand.cuh", "common.cuh", "pipeline.cuh"],
     "expert_ffn_gemm": ["gemm_sm103.cu", "operand.cuh", "tcgen05.cuh", "common.cuh", "pipeline.cuh"],
@@ -972,8 +1019,17 @@ def measure_layer(L, dev, steps, warmup, flush, stream, pg, e2e=True, clk=None):
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    if clk is not None:  # clocks sampled during the timed region only
+    if clk is not None:
+        # clocks: the sampler starts ahead of the timed steps (nvidia-smi takes ~0.1 s to
+        # give its first sample, more than a short timed region lasts) and runs through
+        # CLOCK_PREROLL_S of untimed replays of the same step, then the timed steps
         with clk:
+            clk.window = f"{CLOCK_PREROLL_S:.1f} s of untimed replays of the timed step, then the timed steps"
+            t_end = time.time() + CLOCK_PREROLL_S
+            while time.time() < t_end:
+                for _ in range(16):
+                    graph.replay()
+                torch.cuda.synchronize()
             step_ms = timed(graph.replay, steps)
     else:
         step_ms = timed(graph.replay, steps)

@@ -114,13 +114,36 @@ def test_clock_sampler_reads_nvml_often_and_maps_reasons(monkeypatch):
 
 
 def test_clock_sampler_falls_back_without_nvml(monkeypatch):
+    """Without NVML the sampler reads one nvidia-smi process in loop mode (a fake here)
+    until the timed region ends, then ends that process."""
     import sys
+    import time
     monkeypatch.setitem(sys.modules, "pynvml", None)  # import fails
+    line = "0, 2032, 2032, 800.00, 0x4, Not Active, Not Active, Not Active, Active\n"
+    ended = {"terminated": False}
+
+    class FakeProc:
+        def __init__(self, argv, **kw):
+            assert argv[0] == "nvidia-smi" and "-lms" in argv
+            self.stdout = self._lines()
+
+        def _lines(self):
+            for _ in range(1000):
+                if ended["terminated"]:
+                    return
+                time.sleep(0.005)
+                yield line
+
+        def terminate(self):
+            ended["terminated"] = True
+
+        def wait(self, timeout=None):
+            return 0
+    monkeypatch.setattr(bench.subprocess, "Popen", FakeProc)
     clk = bench.ClockSampler(0)
-    monkeypatch.setattr(clk, "_smi_row", lambda: ["0", "2032", "2032", "800.00", "0x0",
-                                                  "Not Active", "Not Active", "Not Active", "Active"])
     with clk:
-        import time
         time.sleep(0.05)
     s = clk.summary()
-    assert s["source"] == "nvidia-smi" and s["samples"] >= 1 and s["reasons"] == ["sw_power_cap"]
+    assert ended["terminated"]
+    assert s["source"] == "nvidia-smi" and s["samples"] >= 3 and s["reasons"] == ["sw_power_cap"]
+    assert s["sm_mhz"] == 2032.0
